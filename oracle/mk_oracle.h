@@ -1,0 +1,72 @@
+/*
+ * mk_oracle.h -- plain, slow CPU oracle for MoE top-k routing, dispatch and
+ * the per-expert GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may call this library.  It shares no code,
+ * header, table or helper with the CUDA library: it is an independent
+ * restatement of what the path computes, used to check it.
+ *
+ * The pages ("mKernel: UCCL fuses NVLink, RDMA and compute into one
+ * persistent CUDA kernel", zubnet.ai, para. 2; "mKernel : une bibliotheque
+ * de noyaux fusionnes ...", lefilia.fr, paras. 1 and 3) name the operation
+ * "MoE Dispatch+GEMM" -- tokens routed dynamically to experts, then the
+ * expert's dense product -- but print none of its steps.  The steps below are
+ * the textbook top-k MoE routing definition, stated in full:
+ *
+ *   1. For each token t, order the experts by the key (-logit, expert id)
+ *      ascending and keep the first k as slots j = 0..k-1 (descending logit,
+ *      ties to the lower expert id; -inf is a legal logit).
+ *   2. gate[t,j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k chosen
+ *      logits, in fp64, rounded to f32.  A -inf logit gets gate 0; if all k
+ *      chosen logits are -inf every gate is 0.
+ *   3. count[e] = number of (t,j) with idx[t,j] = e.
+ *   4. expert_offsets = exclusive scan of count; offsets[E] = T*k.
+ *   5. Sorted rows are all (t,j) pairs ordered by (e, t, j).
+ *   6. src_index[r] = t*k + j;  gate_w[r] = gate[t,j].
+ *   7. y[r,f] = sum_h x[t,h] * W[e,h,f], accumulated in fp64 in ascending h.
+ *
+ * Inputs that are NaN or +inf are outside the contract: every function
+ * returns MKO_EBADVAL for them.
+ *
+ * Error returns: 0 on success; MKO_EARG for bad sizes or null pointers;
+ * MKO_EBADVAL for logits outside the contract.
+ */
+#ifndef MK_ORACLE_H
+#define MK_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MKO_OK 0
+#define MKO_EARG 1
+#define MKO_EBADVAL 2
+
+/* Step 1-2.  logits[T,E] f32 row-major -> topk_idx[T,k] i32, topk_gate[T,k] f32. */
+int mko_route(const float* logits, int64_t T, int E, int k,
+              int32_t* topk_idx, float* topk_gate);
+
+/* Steps 3-6.  From the routing result to expert_offsets[E+1], src_index[T*k],
+ * gate_w[T*k] (both in sorted-row order). */
+int mko_dispatch(const int32_t* topk_idx, const float* topk_gate,
+                 int64_t T, int E, int k,
+                 int32_t* expert_offsets, int32_t* src_index, float* gate_w);
+
+/* Step 7 for a list of sorted rows.  x[T,H] and W[E,H,F] are bf16 bit
+ * patterns (uint16), row-major.  rows[n] are indices into the sorted order;
+ * y[n,F] receives the fp64 products. */
+int mko_expert_rows(const uint16_t* x, const uint16_t* W,
+                    int64_t T, int H, int F, int E, int k,
+                    const int32_t* expert_offsets, const int32_t* src_index,
+                    const int64_t* rows, int64_t n, double* y);
+
+/* Number of threads the oracle's parallel loops use. */
+int mko_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

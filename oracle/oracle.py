@@ -1,0 +1,126 @@
+"""ctypes front end of the C oracle (TEST INFRASTRUCTURE ONLY).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg use this module.  It never imports the CUDA library or its binding; its
+inputs come from the seeded generator in ``synth.py``.
+
+The oracle computes top-k MoE routing, dispatch and the per-expert product
+as written out in ``mk_oracle.h`` (the pages name "MoE Dispatch+GEMM" and
+dynamic token routing to experts but print no steps).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIBS: dict[str, ctypes.CDLL] = {}
+
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_p = ctypes.c_void_p
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building if needed) the oracle library; ``path`` selects a variant build."""
+    path = path or _build.build()
+    lib = _LIBS.get(path)
+    if lib is None:
+        lib = ctypes.CDLL(path)
+        lib.mko_route.argtypes = [_p, _i64, _int, _int, _p, _p]
+        lib.mko_dispatch.argtypes = [_p, _p, _i64, _int, _int, _p, _p, _p]
+        lib.mko_expert_rows.argtypes = [_p, _p, _i64, _int, _int, _int, _int, _p, _p, _p, _i64, _p]
+        for f in (lib.mko_route, lib.mko_dispatch, lib.mko_expert_rows):
+            f.restype = _int
+        lib.mko_num_threads.restype = _int
+        _LIBS[path] = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise OracleError(f"{what} returned {rc}")
+
+
+class Oracle:
+    """Thin object wrapper so a test can point at a variant build of the oracle."""
+
+    def __init__(self, path: str | None = None):
+        self.lib = load(path)
+
+    def num_threads(self) -> int:
+        return int(self.lib.mko_num_threads())
+
+    def route(self, logits: np.ndarray, k: int):
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        T, E = logits.shape
+        idx = np.zeros((T, k), dtype=np.int32)
+        gate = np.zeros((T, k), dtype=np.float32)
+        _check(self.lib.mko_route(_ptr(logits), T, E, k, _ptr(idx), _ptr(gate)), "mko_route")
+        return idx, gate
+
+    def dispatch(self, idx: np.ndarray, gate: np.ndarray, E: int):
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        gate = np.ascontiguousarray(gate, dtype=np.float32)
+        T, k = idx.shape
+        offsets = np.zeros(E + 1, dtype=np.int32)
+        src = np.zeros(T * k, dtype=np.int32)
+        gw = np.zeros(T * k, dtype=np.float32)
+        _check(self.lib.mko_dispatch(_ptr(idx), _ptr(gate), T, E, k, _ptr(offsets), _ptr(src), _ptr(gw)),
+               "mko_dispatch")
+        return offsets, src, gw
+
+    def expert_rows(self, x_bits, W_bits, k, offsets, src, rows):
+        """fp64 y for the sorted rows ``rows``; x_bits[T,H], W_bits[E,H,F] uint16 bf16 bits."""
+        x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        W_bits = np.ascontiguousarray(W_bits, dtype=np.uint16)
+        T, H = x_bits.shape
+        E, H2, F = W_bits.shape
+        assert H2 == H
+        offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+        src = np.ascontiguousarray(src, dtype=np.int32)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        y = np.zeros((rows.size, F), dtype=np.float64)
+        _check(self.lib.mko_expert_rows(_ptr(x_bits), _ptr(W_bits), T, H, F, E, k, _ptr(offsets), _ptr(src),
+                                        _ptr(rows), rows.size, _ptr(y)), "mko_expert_rows")
+        return y
+
+    def full(self, x_bits, logits, W_bits, k, rows=None):
+        """Every output of the path; ``rows`` limits the fp64 product to a sample."""
+        E = W_bits.shape[0]
+        idx, gate = self.route(logits, k)
+        offsets, src, gw = self.dispatch(idx, gate, E)
+        if rows is None:
+            rows = np.arange(src.size, dtype=np.int64)
+        y = self.expert_rows(x_bits, W_bits, k, offsets, src, rows)
+        return dict(topk_idx=idx, topk_gate=gate, expert_offsets=offsets, src_index=src, gate_w=gw,
+                    rows=np.asarray(rows, dtype=np.int64), y=y)
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def oracle_threads() -> int:
+    return default().num_threads()
+
+
+def lib_path() -> str:
+    return os.path.abspath(_build.build())

@@ -1,0 +1,166 @@
+/*
+ * mk.h -- C ABI of the GB300 (sm_103a) MoE token dispatch + expert GEMM.
+ *
+ * What the operation is.  The mKernel write-ups name "MoE Dispatch+GEMM" as
+ * one of five fused persistent kernels: tokens are routed dynamically to
+ * experts and each expert's dense product runs as soon as its tile of tokens
+ * has arrived, inside one kernel ("mKernel: UCCL fuses NVLink, RDMA and
+ * compute into one persistent CUDA kernel", zubnet.ai, paras. 1-2;
+ * "UC Berkeley presenta mKernel ...", edge.aivizor.me, para. 3;
+ * "mKernel : une bibliotheque de noyaux fusionnes ...", lefilia.fr,
+ * paras. 1 and 3).  The pages print none of the steps, so this header
+ * states the contract the library implements:
+ *
+ *   1. Router top-k.  For token t, the k experts with the largest logits,
+ *      in descending order, ties to the lower expert id; -inf is a legal
+ *      logit (NaN and +inf are outside the contract: results unspecified,
+ *      no fault).
+ *   2. Gates.  gate[t,j] = softmax over the k chosen logits (fp32 expf);
+ *      a -inf logit gets 0; if all k chosen are -inf every gate is 0.
+ *   3. expert_offsets[e] = number of (t,j) routed to experts < e
+ *      (exclusive scan of the per-expert histogram); expert_offsets[E] = T*k.
+ *   4. Sorted rows: every (t,j) pair, ordered by (expert, t, j).  For sorted
+ *      row r: src_index[r] = t*k + j, gate_w[r] = gate[t,j].
+ *   5. y_sorted[r,:] = x[t,:] . W[e,:,:] with fp32 accumulation, stored as
+ *      bf16 (round-to-nearest-even) or, with MK_OUT_F32, as fp32.  Rows are
+ *      not scaled by the gate.
+ *
+ * Layouts (all row-major, caller-owned, device memory unless stated):
+ *   x[T,H] bf16, logits[T,E] f32, W[E,H,F] bf16 (F contiguous)   -- read only
+ *   y_sorted[T*k,F] bf16 (or f32), src_index[T*k] i32,
+ *   expert_offsets[E+1] i32, gate_w[T*k] f32                     -- written
+ *   bf16 travels as 16-bit storage (void*); the library never frees caller
+ *   memory.
+ *
+ * Limits (checked synchronously, no launch on failure -> MK_ERR_INVALID_ARG
+ * or MK_ERR_UNSUPPORTED): T >= 0; 1 <= k <= min(E, 8); 1 <= E <= 256;
+ * H and F multiples of 64 in [64, 32768]; T*k < 2^31; x, W, y_sorted 16-byte
+ * aligned, the other arrays 4-byte aligned; the current device must be
+ * sm_103 (compute capability 10.3).  T == 0 is valid: expert_offsets is set
+ * to zeros and nothing else is written.
+ *
+ * Asynchrony.  Calls enqueue work on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and return without synchronising.  A fault or a
+ * bounded wait that ran out inside the kernel is recorded in a per-device
+ * error word; mk_get_status() synchronises the stream and reports it.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MK_OK = 0,
+    MK_ERR_INVALID_ARG = 1,   /* bad size, null or misaligned pointer      */
+    MK_ERR_UNSUPPORTED = 2,   /* wrong device, or shape beyond the limits  */
+    MK_ERR_CUDA = 3,          /* a CUDA runtime call failed                */
+    MK_ERR_TIMEOUT = 4,       /* a bounded device wait ran out             */
+    MK_ERR_DEVICE_FAULT = 5,  /* the kernel detected an inconsistent state */
+    MK_ERR_NOT_IMPLEMENTED = 6,
+    MK_ERR_WORKSPACE = 7      /* caller workspace too small or misaligned  */
+} mk_status_t;
+
+/* Execution modes. */
+enum {
+    MK_MODE_FUSED = 0,         /* one persistent launch: dispatch and compute roles overlap per tile */
+    MK_MODE_UNFUSED = 1,       /* the same steps as four launches (route, scan, gather, GEMM)       */
+    MK_MODE_DISPATCH_ONLY = 2  /* routing + gather only (y_sorted untouched); measures dispatch      */
+};
+
+enum { MK_OUT_BF16 = 0, MK_OUT_F32 = 1 };
+
+/* Host-side fault injection (never a device trap): withhold the readiness
+ * flag of one tile so the compute role's bounded wait runs out. */
+enum { MK_FAULT_NONE = 0, MK_FAULT_DROP_TILE_FLAG = 1 };
+
+typedef struct mk_config {
+    int32_t mode;           /* MK_MODE_*                                        */
+    int32_t out_dtype;      /* MK_OUT_BF16 or MK_OUT_F32                         */
+    int32_t dispatch_ctas;  /* CTAs in the dispatch role; 0 = shape heuristic    */
+    int32_t grid_ctas;      /* persistent grid size; 0 = one CTA per SM          */
+    int32_t n_group;        /* N-blocks per group in the work order; 0 = auto    */
+    int32_t debug_fault;    /* MK_FAULT_*                                        */
+    int64_t spin_limit_ns;  /* bound on every device wait; 0 = 2 s               */
+    int32_t trace;          /* 1 = record per-CTA %globaltimer phase stamps      */
+    int32_t reserved[7];    /* must be zero                                     */
+} mk_config_t;
+
+/* Per-launch facts, for tests and the benchmark. */
+typedef struct mk_launch_info {
+    int32_t grid_ctas;      /* CTAs launched by the persistent kernel */
+    int32_t dispatch_ctas;  /* of which in the dispatch role          */
+    int32_t launches;       /* kernels launched by the last call      */
+    int32_t n_group;
+    int64_t workspace_bytes;
+} mk_launch_info_t;
+
+/* Fill `cfg` with the defaults (fused, bf16 output, heuristic split). */
+void mk_config_default(mk_config_t* cfg);
+
+/* The fused path with default configuration and the library's
+ * per-(device, stream) workspace cache.  Device pointers; see above. */
+mk_status_t mk_moe_dispatch_gemm(const void* x, const float* logits, int T, int H, int E, int k,
+                                 const void* W, int F, void* y_sorted, int32_t* src_index,
+                                 int32_t* expert_offsets, float* gate_w, void* stream);
+
+/* As mk_moe_dispatch_gemm with an explicit configuration (NULL = defaults)
+ * and an optional caller workspace.  With workspace == NULL the library's
+ * cache is used (grown with cudaMallocAsync on `stream`).  A caller
+ * workspace must hold mk_workspace_size() bytes, be 256-byte aligned, and be
+ * zero-filled before its first use (the kernels leave it ready for the next
+ * call).  One workspace serves one stream at a time. */
+mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, int H, int E, int k,
+                                    const void* W, int F, void* y_sorted, int32_t* src_index,
+                                    int32_t* expert_offsets, float* gate_w, void* stream,
+                                    const mk_config_t* cfg, void* workspace, size_t ws_bytes);
+
+/* End-to-end variant: x, logits and the four outputs are HOST buffers
+ * (pinned memory gives asynchronous copies); W stays on the device (expert
+ * weights are resident).  Copies the inputs in, runs the fused path, copies
+ * the outputs back, and synchronises `stream` before returning, so the host
+ * buffers are ready on return.  Device staging comes from the library cache. */
+mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_host, int T, int H, int E,
+                                      int k, const void* W, int F, void* y_sorted_host,
+                                      int32_t* src_index_host, int32_t* expert_offsets_host,
+                                      float* gate_w_host, void* stream, const mk_config_t* cfg);
+
+/* Bytes of workspace a call with these sizes needs (0 on invalid sizes). */
+size_t mk_workspace_size(int T, int H, int F, int E, int k, const mk_config_t* cfg);
+
+/* Synchronise `stream`, then return and clear the device error word
+ * (MK_ERR_TIMEOUT / MK_ERR_DEVICE_FAULT), or MK_ERR_CUDA if the stream holds
+ * a CUDA error.  MK_OK when nothing was recorded. */
+mk_status_t mk_get_status(void* stream);
+
+/* Detail of the last recorded device error: site code and CTA (or -1). */
+void mk_last_error_detail(int32_t* site, int32_t* cta, int32_t* info);
+
+/* Facts about the last call on this thread (grid, role split, launches). */
+void mk_last_launch_info(mk_launch_info_t* info);
+
+/* Copy the phase stamps of the last traced call (cfg.trace = 1) made with
+ * these sizes on `stream` to the host: up to n uint64 values, 16 per CTA
+ * (%globaltimer ns; 0 = phase not reached).  `workspace` is the caller
+ * workspace that call used, or NULL for the library cache of `stream`.
+ * Synchronises `stream`. */
+mk_status_t mk_read_trace(void* stream, const void* workspace, int T, int H, int E, int k, uint64_t* out,
+                          size_t n);
+
+/* Free the library's workspace cache on every device (synchronises). */
+void mk_release_workspace(void);
+
+/* Static string for a status code. */
+const char* mk_status_string(mk_status_t s);
+
+/* Library ABI version (major * 100 + minor). */
+int mk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

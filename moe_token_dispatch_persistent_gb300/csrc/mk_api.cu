@@ -1,0 +1,466 @@
+// mk_api.cu -- host side of the C ABI declared in include/mk.h: argument
+// validation, the per-(device, stream) workspace cache, TMA tensor maps, the
+// role split between dispatch and compute CTAs, and error reporting.
+//
+// The split follows the mKernel design note that the number of SMs given to
+// each CTA role is set from the tensor shapes ("UC Berkeley presenta mKernel
+// ...", edge.aivizor.me, para. 3; lefilia.fr, para. 2): here it is the share
+// of the gather's HBM time in the path's total time.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "mk.h"
+#include "mk_common.h"
+
+namespace mk {
+cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st);
+cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st);
+cudaError_t set_kernel_attributes();
+cudaError_t fused_max_blocks_per_sm(int* n);
+cudaError_t read_and_clear_error(uint32_t out[4], cudaStream_t st);
+}  // namespace mk
+
+using namespace mk;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultSpinNs = 2000000000LL;
+
+struct DevInfo {
+    bool ready = false;
+    mk_status_t status = MK_OK;
+    int sms = 0;
+    int max_blocks = 0;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+thread_local mk_launch_info_t g_last_info{};
+uint32_t g_last_err[4] = {0, 0, 0, 0};
+
+struct WsEntry {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
+
+struct HostStage {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, HostStage> g_host_stage;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+mk_status_t device_info(int* dev_out, DevInfo** info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MK_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MK_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            return MK_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
+            d.status = MK_ERR_UNSUPPORTED;
+        } else if (set_kernel_attributes() != cudaSuccess || fused_max_blocks_per_sm(&d.max_blocks) != cudaSuccess) {
+            return MK_ERR_CUDA;
+        } else if (d.max_blocks < 1) {
+            d.status = MK_ERR_UNSUPPORTED;
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q{};
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return MK_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *dev_out = dev;
+    *info = &d;
+    return d.status;
+}
+
+mk_status_t validate_sizes(int T, int H, int E, int k, int F) {
+    if (T < 0 || E < 1 || k < 1 || k > E || k > MAX_K) return MK_ERR_INVALID_ARG;
+    if (E > MAX_E) return MK_ERR_UNSUPPORTED;
+    if (H < 64 || F < 64 || H % 64 != 0 || F % 64 != 0) return MK_ERR_INVALID_ARG;
+    if (H > 32768 || F > 32768) return MK_ERR_UNSUPPORTED;
+    if (int64_t(T) * k >= (int64_t(1) << 31)) return MK_ERR_UNSUPPORTED;
+    if (int64_t(E) * H >= (int64_t(1) << 31)) return MK_ERR_UNSUPPORTED;
+    return MK_OK;
+}
+
+mk_config_t config_or_default(const mk_config_t* cfg) {
+    mk_config_t c;
+    mk_config_default(&c);
+    if (cfg) c = *cfg;
+    return c;
+}
+
+int grid_for(const DevInfo& d, const mk_config_t& c) {
+    int grid = d.sms * (d.max_blocks > 0 ? d.max_blocks : 1);
+    grid = grid > d.sms ? d.sms : grid;  // one CTA per SM: each holds ~200 KB smem and 512 TMEM columns
+    if (c.grid_ctas > 0 && c.grid_ctas < grid) grid = c.grid_ctas;
+    if (grid > MAX_GRID) grid = MAX_GRID;
+    return grid;
+}
+
+// Role split from the shapes: the dispatch role gets the gather's share of
+// the path's estimated time (row bytes moved at HBM rate vs. the FLOPs at
+// tensor rate), at least 4 CTAs and at most half of the grid.  Dispatch CTAs
+// join the compute role once the gather queue is empty.
+int dispatch_split(int grid, int T, int H, int F, int k) {
+    const double rows = double(T) * k;
+    const double gather_s = rows * H * 4.0 / 6.0e12;
+    const double gemm_s = 2.0 * rows * H * double(F) / 1.8e15;
+    int d = int(std::ceil(grid * gather_s / (gather_s + gemm_s)));
+    if (d < 4) d = 4;
+    if (d > grid / 2) d = grid / 2;
+    if (d < 1) d = 1;
+    return d;
+}
+
+// Work order within an expert: whole expert weight reused through L2 when it
+// is small (N-group = all N-blocks, tiles outer); otherwise groups of
+// N-blocks whose weight slice is ~16 MB.
+int n_group_for(int H, int F, int nb) {
+    const double w_bytes = double(H) * F * 2.0;
+    if (w_bytes <= 32.0 * 1024 * 1024) return nb;
+    int g = int((16.0 * 1024 * 1024) / (double(H) * BN * 2.0));
+    if (g < 1) g = 1;
+    if (g > nb) g = nb;
+    return g;
+}
+
+CUresult encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                   uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// The library's workspace for (device, stream), grown on demand.  The new
+// buffer's bookkeeping part (everything before the staging rows) is zeroed.
+mk_status_t cached_workspace(int dev, cudaStream_t st, size_t need, size_t zero_bytes, void** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    WsEntry& w = g_ws[{dev, st}];
+    if (w.bytes < need) {
+        if (w.ptr && cudaFreeAsync(w.ptr, st) != cudaSuccess) return MK_ERR_CUDA;
+        w.ptr = nullptr;
+        w.bytes = 0;
+        size_t grow = need + need / 4;
+        if (cudaMallocAsync(&w.ptr, grow, st) != cudaSuccess) {
+            w.ptr = nullptr;
+            return MK_ERR_CUDA;
+        }
+        if (cudaMemsetAsync(w.ptr, 0, zero_bytes, st) != cudaSuccess) return MK_ERR_CUDA;
+        w.bytes = grow;
+    }
+    *out = w.ptr;
+    return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void mk_config_default(mk_config_t* cfg) {
+    if (!cfg) return;
+    std::memset(cfg, 0, sizeof(*cfg));
+    cfg->mode = MK_MODE_FUSED;
+    cfg->out_dtype = MK_OUT_BF16;
+}
+
+int mk_version(void) { return 100; }
+
+const char* mk_status_string(mk_status_t s) {
+    switch (s) {
+        case MK_OK: return "MK_OK";
+        case MK_ERR_INVALID_ARG: return "MK_ERR_INVALID_ARG";
+        case MK_ERR_UNSUPPORTED: return "MK_ERR_UNSUPPORTED";
+        case MK_ERR_CUDA: return "MK_ERR_CUDA";
+        case MK_ERR_TIMEOUT: return "MK_ERR_TIMEOUT";
+        case MK_ERR_DEVICE_FAULT: return "MK_ERR_DEVICE_FAULT";
+        case MK_ERR_NOT_IMPLEMENTED: return "MK_ERR_NOT_IMPLEMENTED";
+        case MK_ERR_WORKSPACE: return "MK_ERR_WORKSPACE";
+    }
+    return "MK_ERR_UNKNOWN";
+}
+
+size_t mk_workspace_size(int T, int H, int F, int E, int k, const mk_config_t* cfg) {
+    (void)cfg;
+    if (validate_sizes(T, H, E, k, F) != MK_OK) return 0;
+    return ws_layout(T, H, E, k).total;
+}
+
+mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, int H, int E, int k, const void* W,
+                                    int F, void* y_sorted, int32_t* src_index, int32_t* expert_offsets,
+                                    float* gate_w, void* stream, const mk_config_t* cfg_in, void* workspace,
+                                    size_t ws_bytes) {
+    g_last_info = mk_launch_info_t{};
+    mk_status_t s = validate_sizes(T, H, E, k, F);
+    if (s != MK_OK) return s;
+    const mk_config_t c = config_or_default(cfg_in);
+    for (int i = 0; i < 7; ++i)
+        if (c.reserved[i] != 0) return MK_ERR_INVALID_ARG;
+    if (c.mode < MK_MODE_FUSED || c.mode > MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
+    if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
+    if (c.debug_fault != MK_FAULT_NONE && c.debug_fault != MK_FAULT_DROP_TILE_FLAG) return MK_ERR_INVALID_ARG;
+    if (c.dispatch_ctas < 0 || c.grid_ctas < 0 || c.n_group < 0 || c.spin_limit_ns < 0) return MK_ERR_INVALID_ARG;
+    if (!expert_offsets || !aligned(expert_offsets, 4)) return MK_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!x || !logits || !W || !src_index || !gate_w) return MK_ERR_INVALID_ARG;
+        if (!y_sorted && c.mode != MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
+        if (!aligned(x, 16) || !aligned(W, 16) || !aligned(logits, 4) || !aligned(src_index, 4) ||
+            !aligned(gate_w, 4))
+            return MK_ERR_INVALID_ARG;
+        if (y_sorted && !aligned(y_sorted, 16)) return MK_ERR_INVALID_ARG;
+    }
+    int dev = 0;
+    DevInfo* d = nullptr;
+    if ((s = device_info(&dev, &d)) != MK_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (T == 0) {
+        g_last_info.launches = 0;
+        return cudaMemsetAsync(expert_offsets, 0, size_t(E + 1) * 4, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    }
+
+    const int grid = grid_for(*d, c);
+    const int rows = T * k;
+    const int nch = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    if (nch > grid * MAX_CHUNKS_PER_CTA) return MK_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(T, H, E, k);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (ws) {
+        if (ws_bytes < L.total || !aligned(ws, 256)) return MK_ERR_WORKSPACE;
+    } else {
+        void* p = nullptr;
+        if ((s = cached_workspace(dev, st, L.total, L.xs, &p)) != MK_OK) return s;
+        ws = static_cast<uint8_t*>(p);
+    }
+
+    Params p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.logits = logits;
+    p.W = static_cast<const uint16_t*>(W);
+    p.y = y_sorted;
+    p.src_index = src_index;
+    p.expert_offsets = expert_offsets;
+    p.gate_w = gate_w;
+    p.T = T;
+    p.H = H;
+    p.F = F;
+    p.E = E;
+    p.k = k;
+    p.out_f32 = c.out_dtype == MK_OUT_F32;
+    p.rows = rows;
+    p.nch = nch;
+    p.nb = (F + BN - 1) / BN;
+    p.kblocks = H / BK;
+    p.n_group = c.n_group > 0 ? (c.n_group < p.nb ? c.n_group : p.nb) : n_group_for(H, F, p.nb);
+    p.mode = c.mode;
+    p.compute = c.mode != MK_MODE_DISPATCH_ONLY;
+    if (c.mode == MK_MODE_DISPATCH_ONLY) {
+        p.dispatch_ctas = grid;
+    } else {
+        p.dispatch_ctas = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
+        if (p.dispatch_ctas > grid) p.dispatch_ctas = grid;
+    }
+    {
+        int slots = int((SM_STAGE_END) / (size_t(H) * 2));
+        p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
+    }
+    p.debug_drop_tile = c.debug_fault == MK_FAULT_DROP_TILE_FLAG ? 0 : -1;
+    p.trace = c.trace ? 1 : 0;
+    p.spin_limit_ns = c.spin_limit_ns > 0 ? c.spin_limit_ns : kDefaultSpinNs;
+    p.ctl = reinterpret_cast<Ctl*>(ws + L.ctl);
+    p.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+    p.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
+    p.topk_gate = reinterpret_cast<float*>(ws + L.topk_gate);
+    p.lrank = reinterpret_cast<int32_t*>(ws + L.lrank);
+    p.bases = reinterpret_cast<int32_t*>(ws + L.bases);
+    p.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
+    p.xs = reinterpret_cast<uint16_t*>(ws + L.xs);
+    p.trace_buf = reinterpret_cast<unsigned long long*>(ws + L.trace);
+    p.max_tiles = (rows + BM - 1) / BM + E;
+
+    CUtensorMap tmA, tmB;
+    std::memset(&tmA, 0, sizeof(tmA));
+    std::memset(&tmB, 0, sizeof(tmB));
+    if (encode_2d(&tmA, p.xs, uint64_t(H), uint64_t(rows), uint64_t(H) * 2, BK, BM) != CUDA_SUCCESS)
+        return MK_ERR_CUDA;
+    if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+        return MK_ERR_CUDA;
+
+    if (p.trace && cudaMemsetAsync(p.trace_buf, 0, size_t(grid) * TRACE_SLOTS * 8, st) != cudaSuccess)
+        return MK_ERR_CUDA;
+
+    cudaError_t err;
+    if (c.mode == MK_MODE_UNFUSED) {
+        err = launch_unfused(p, tmA, tmB, grid, st);
+        g_last_info.launches = 4;
+    } else {
+        err = launch_fused(p, tmA, tmB, grid, st);
+        g_last_info.launches = 1;
+    }
+    g_last_info.grid_ctas = grid;
+    g_last_info.dispatch_ctas = c.mode == MK_MODE_UNFUSED ? 0 : p.dispatch_ctas;
+    g_last_info.n_group = p.n_group;
+    g_last_info.workspace_bytes = int64_t(L.total);
+    if (getenv("MK_LOG"))
+        fprintf(stderr, "[mk] T=%d H=%d F=%d E=%d k=%d mode=%d grid=%d dispatch=%d n_group=%d slots=%d ws=%zu\n", T, H,
+                F, E, k, c.mode, grid, p.dispatch_ctas, p.n_group, p.gather_slots, L.total);
+    return err == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
+mk_status_t mk_moe_dispatch_gemm(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,
+                                 void* y_sorted, int32_t* src_index, int32_t* expert_offsets, float* gate_w,
+                                 void* stream) {
+    return mk_moe_dispatch_gemm_ex(x, logits, T, H, E, k, W, F, y_sorted, src_index, expert_offsets, gate_w, stream,
+                                   nullptr, nullptr, 0);
+}
+
+mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_host, int T, int H, int E, int k,
+                                      const void* W, int F, void* y_sorted_host, int32_t* src_index_host,
+                                      int32_t* expert_offsets_host, float* gate_w_host, void* stream,
+                                      const mk_config_t* cfg) {
+    mk_status_t s = validate_sizes(T, H, E, k, F);
+    if (s != MK_OK) return s;
+    const mk_config_t c = config_or_default(cfg);
+    if (!expert_offsets_host) return MK_ERR_INVALID_ARG;
+    if (T > 0 && (!x_host || !logits_host || !W || !y_sorted_host || !src_index_host || !gate_w_host))
+        return MK_ERR_INVALID_ARG;
+    int dev = 0;
+    DevInfo* d = nullptr;
+    if ((s = device_info(&dev, &d)) != MK_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t rows = size_t(T) * k;
+    const size_t ybytes = rows * F * (c.out_dtype == MK_OUT_F32 ? 4 : 2);
+    const size_t o_x = 0, o_l = ws_align(o_x + size_t(T) * H * 2), o_y = ws_align(o_l + size_t(T) * E * 4),
+                 o_s = ws_align(o_y + ybytes), o_o = ws_align(o_s + rows * 4), o_g = ws_align(o_o + size_t(E + 1) * 4),
+                 total = ws_align(o_g + rows * 4);
+    uint8_t* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        HostStage& h = g_host_stage[{dev, st}];
+        if (h.bytes < total) {
+            if (h.ptr && cudaFreeAsync(h.ptr, st) != cudaSuccess) return MK_ERR_CUDA;
+            h.ptr = nullptr;
+            h.bytes = 0;
+            if (cudaMallocAsync(&h.ptr, total, st) != cudaSuccess) return MK_ERR_CUDA;
+            h.bytes = total;
+        }
+        base = static_cast<uint8_t*>(h.ptr);
+    }
+    if (T > 0) {
+        if (cudaMemcpyAsync(base + o_x, x_host, size_t(T) * H * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(base + o_l, logits_host, size_t(T) * E * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return MK_ERR_CUDA;
+    }
+    s = mk_moe_dispatch_gemm_ex(base + o_x, reinterpret_cast<const float*>(base + o_l), T, H, E, k, W, F, base + o_y,
+                                reinterpret_cast<int32_t*>(base + o_s), reinterpret_cast<int32_t*>(base + o_o),
+                                reinterpret_cast<float*>(base + o_g), stream, &c, nullptr, 0);
+    if (s != MK_OK) return s;
+    if (cudaMemcpyAsync(expert_offsets_host, base + o_o, size_t(E + 1) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MK_ERR_CUDA;
+    if (T > 0) {
+        if (cudaMemcpyAsync(y_sorted_host, base + o_y, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaMemcpyAsync(src_index_host, base + o_s, rows * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaMemcpyAsync(gate_w_host, base + o_g, rows * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return MK_ERR_CUDA;
+    }
+    return mk_get_status(stream);
+}
+
+mk_status_t mk_get_status(void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+    uint32_t e[4] = {0, 0, 0, 0};
+    if (read_and_clear_error(e, st) != cudaSuccess) return MK_ERR_CUDA;
+    if (e[0] == ERR_NONE) return MK_OK;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        std::memcpy(g_last_err, e, sizeof(e));
+    }
+    return e[0] == ERR_TIMEOUT ? MK_ERR_TIMEOUT : MK_ERR_DEVICE_FAULT;
+}
+
+void mk_last_error_detail(int32_t* site, int32_t* cta, int32_t* info) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (site) *site = int32_t(g_last_err[1]);
+    if (cta) *cta = int32_t(g_last_err[2]);
+    if (info) *info = int32_t(g_last_err[3]);
+}
+
+void mk_last_launch_info(mk_launch_info_t* info) {
+    if (info) *info = g_last_info;
+}
+
+mk_status_t mk_read_trace(void* stream, const void* workspace, int T, int H, int E, int k, uint64_t* out, size_t n) {
+    if (!out) return MK_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MK_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+    if (!ws) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_ws.find({dev, st});
+        if (it == g_ws.end()) return MK_ERR_INVALID_ARG;
+        ws = static_cast<const uint8_t*>(it->second.ptr);
+    }
+    const WsLayout L = ws_layout(T, H, E, k);
+    const size_t want = size_t(MAX_GRID) * TRACE_SLOTS;
+    const size_t cnt = n < want ? n : want;
+    if (cudaMemcpyAsync(out, ws + L.trace, cnt * 8, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MK_ERR_CUDA;
+    return cudaStreamSynchronize(st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
+void mk_release_workspace(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    // streams may be gone by now: synchronise the device, then free
+    for (auto& kv : g_ws) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaDeviceSynchronize();
+        cudaFree(kv.second.ptr);
+    }
+    g_ws.clear();
+    for (auto& kv : g_host_stage) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaDeviceSynchronize();
+        cudaFree(kv.second.ptr);
+    }
+    g_host_stage.clear();
+    cudaSetDevice(cur);
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+// mk_common.h -- constants and parameter blocks shared by the host launcher
+// and the device code of the MoE dispatch + expert-GEMM library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mk {
+
+// Tile shape of the expert GEMM: one CTA computes a BM x BN block of
+// y_sorted with tcgen05.mma (M = 128, N = 256, K = 16 per instruction),
+// K staged through shared memory BK = 64 bf16 (one 128-byte swizzle row).
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;            // 16 KiB
+constexpr int B_CHUNK_BYTES = BK * 64 * 2;            //  8 KiB: 64 rows of K x 64 columns of N
+constexpr int B_STAGE_BYTES = BK * BN * 2;            // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;                     // two fp32 accumulators
+constexpr int NWARPS = 6;                             // producer, MMA, 4 x epilogue
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int ROUTE_CHUNK = NWARPS * 32;              // tokens per routing chunk (lane per token)
+constexpr int MAX_E = 256;
+constexpr int MAX_K = 8;
+constexpr int MAX_CHUNKS_PER_CTA = 16;
+constexpr int MAX_GATHER_SLOTS = 32;
+constexpr int TRACE_SLOTS = 16;
+
+// Dynamic shared memory map (offsets from a 1024-byte aligned base).
+constexpr int SM_A = 0;
+constexpr int SM_B = SM_A + STAGES * A_STAGE_BYTES;           // 64 KiB
+constexpr int SM_STAGE_END = SM_B + STAGES * B_STAGE_BYTES;   // 192 KiB
+constexpr int SM_CTRL = SM_STAGE_END;
+constexpr int SM_CTRL_BYTES = 8192;
+constexpr int SMEM_BYTES = SM_CTRL + SM_CTRL_BYTES + 1024;    // + alignment slack
+
+// Routing scratch aliases the stage area (routing ends before the GEMM).
+constexpr int RT_LOGIT_STRIDE = 65;                           // 64 experts per pass + 1 pad
+constexpr int RT_LOGITS = 0;
+constexpr int RT_LOGITS_BYTES = NWARPS * 32 * RT_LOGIT_STRIDE * 4;
+constexpr int RT_IDX = RT_LOGITS + RT_LOGITS_BYTES;
+constexpr int RT_LRANK = RT_IDX + NWARPS * 32 * MAX_K * 4;
+constexpr int RT_WCNT = RT_LRANK + NWARPS * 32 * MAX_K * 4;
+constexpr int RT_BASES = RT_WCNT + NWARPS * MAX_E * 4;
+constexpr int RT_END = RT_BASES + MAX_CHUNKS_PER_CTA * MAX_E * 4;
+static_assert(RT_END <= SM_STAGE_END, "routing scratch must fit in the stage area");
+
+// Control block at the head of the workspace.  The kernels leave it ready
+// for the next call: the last CTA to exit zeroes the counters and the abort
+// word.  Readiness flags are cleared by the fused kernel itself.
+struct Ctl {
+    uint32_t epoch;
+    uint32_t exit_count;
+    uint32_t bar_routed;     // CTAs whose routing chunks are written
+    uint32_t bar_scattered;  // CTAs whose src_index / gate_w scatter is written
+    uint32_t next_tile;      // gather queue (dispatch role)
+    uint32_t next_item;      // GEMM work queue (compute role)
+    uint32_t abort;          // 1 once any CTA of this call gave up
+    uint32_t items_done;
+    uint32_t pad[56];
+};
+static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");
+
+enum Mode : int { MODE_FUSED = 0, MODE_UNFUSED = 1, MODE_DISPATCH_ONLY = 2 };
+
+// Error sites recorded with a device error (mk_last_error_detail()).
+enum Site : int {
+    SITE_BAR_ROUTED = 1,
+    SITE_BAR_SCATTERED = 2,
+    SITE_GATHER_LOAD = 3,
+    SITE_TILE_READY = 4,
+    SITE_STAGE_EMPTY = 5,
+    SITE_STAGE_FULL = 6,
+    SITE_ACC_EMPTY = 7,
+    SITE_ACC_FULL = 8,
+    SITE_INFO_FULL = 9,
+    SITE_INFO_EMPTY = 10,
+    SITE_DEST_RANGE = 11,
+    SITE_ROW_TOTAL = 12,
+    SITE_DRAIN = 13,
+};
+
+enum ErrCode : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_FAULT = 2 };
+
+struct Params {
+    // problem (device pointers)
+    const uint16_t* x;       // [T,H] bf16
+    const float* logits;     // [T,E]
+    const uint16_t* W;       // [E,H,F] bf16
+    void* y;                 // [T*k,F] bf16 or f32
+    int32_t* src_index;      // [T*k]
+    int32_t* expert_offsets; // [E+1]
+    float* gate_w;           // [T*k]
+    int T, H, F, E, k;
+    int out_f32;
+    // derived sizes
+    int rows;                // T*k
+    int nch;                 // routing chunks
+    int nb;                  // N-blocks per expert, ceil(F / BN)
+    int kblocks;             // H / BK
+    int n_group;             // N-blocks per group in the work order
+    int dispatch_ctas;       // CTAs [0, dispatch_ctas) take the dispatch role
+    int gather_slots;        // rows in flight per dispatch CTA
+    int mode;
+    int compute;             // 0: dispatch only
+    int debug_drop_tile;     // tile whose flag is withheld (-1: none)
+    int trace;
+    long long spin_limit_ns;
+    // workspace
+    Ctl* ctl;
+    int32_t* counts;         // [nch][E]
+    int32_t* topk_idx;       // [T*k]
+    float* topk_gate;        // [T*k]
+    int32_t* lrank;          // [T*k]
+    int32_t* bases;          // [nch][E] (unfused path)
+    uint32_t* ready;         // [max_tiles]
+    uint16_t* xs;            // [T*k,H] bf16 staging
+    unsigned long long* trace_buf;  // [grid][TRACE_SLOTS]
+    int max_tiles;
+};
+
+// Workspace carve-up, shared by the size query and the launcher.
+struct WsLayout {
+    size_t ctl, counts, topk_idx, topk_gate, lrank, bases, ready, trace, xs, total;
+};
+
+inline size_t ws_align(size_t v) { return (v + 255) & ~size_t(255); }
+
+constexpr int MAX_GRID = 1024;
+
+inline WsLayout ws_layout(int T, int H, int E, int k, int grid = MAX_GRID) {
+    WsLayout L{};
+    const size_t rows = size_t(T) * k;
+    const size_t nch = (size_t(T) + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    const size_t max_tiles = (rows + BM - 1) / BM + E;
+    size_t o = 0;
+    L.ctl = o;        o = ws_align(o + sizeof(Ctl));
+    L.counts = o;     o = ws_align(o + nch * E * 4);
+    L.topk_idx = o;   o = ws_align(o + rows * 4);
+    L.topk_gate = o;  o = ws_align(o + rows * 4);
+    L.lrank = o;      o = ws_align(o + rows * 4);
+    L.bases = o;      o = ws_align(o + nch * E * 4);
+    L.ready = o;      o = ws_align(o + max_tiles * 4);
+    L.trace = o;      o = ws_align(o + size_t(grid) * TRACE_SLOTS * 8);
+    L.xs = o;         o = ws_align(o + rows * size_t(H) * 2);
+    L.total = o;
+    return L;
+}
+
+}  // namespace mk

@@ -1,0 +1,971 @@
+// mk_kernels.cu -- device code of the MoE dispatch + expert GEMM for sm_103a.
+//
+// One persistent kernel (mk_fused_kernel) runs the whole path.  Its CTAs
+// take roles, as the mKernel write-ups describe for their fused kernels
+// (CTAs specialise into compute and communication roles, with the number of
+// SMs per role set from the tensor shapes; "UC Berkeley presenta mKernel
+// ...", edge.aivizor.me, para. 3; lefilia.fr, para. 2), and a tile that has
+// landed feeds the GEMM while the next one is still being moved (zubnet.ai,
+// para. 2).  On one GPU the "communication" role is the gather of token rows
+// from x into expert-contiguous tiles in HBM:
+//
+//   phase R  (all CTAs)    router top-k + gates per token (lane per token),
+//                           per-chunk histogram and stable in-chunk ranks
+//   barrier               every chunk's counts are in
+//   phase S  (all CTAs)    per-expert totals, exclusive scan -> offsets,
+//                           tile and work-item tables (each CTA, in smem);
+//                           scatter src_index / gate_w of the CTA's chunks
+//   dispatch role          pull-gather: tiles taken in GEMM consumption
+//                           order, rows moved with 1-D bulk copies through
+//                           shared memory, a release flag per finished tile;
+//                           then the CTA joins the compute role
+//   compute role           TMA producer warp -> 4-stage mbarrier ring ->
+//                           tcgen05.mma (128x256x16, fp32 in TMEM, double
+//                           buffered) -> 4 epilogue warps (tcgen05.ld,
+//                           bf16/f32 stores of the tile's valid rows)
+//
+// The same device functions also run as four separate launches (route,
+// scan, push-gather, GEMM): the host-driven baseline the fused kernel is
+// measured against.
+//
+// Every wait is bounded (spin_limit_ns, %globaltimer); a wait that runs out
+// records a timeout in the device error word, raises the call's abort flag
+// so the other CTAs stop waiting, drains its own in-flight copies and MMAs,
+// frees TMEM and returns.  Nothing traps.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mk_common.h"
+#include "mk_ptx.cuh"
+
+namespace mk {
+
+struct DevError {
+    uint32_t code, site, cta, info;
+};
+__device__ DevError g_error;
+
+// ------------------------------------------------------------ waiting ------
+
+struct WaitCtx {
+    const uint32_t* abort;
+    uint32_t abort_val;
+    long long limit_ns;
+};
+
+__device__ __noinline__ void record_error(uint32_t code, uint32_t site, uint32_t info) {
+    if (atomicCAS(&g_error.code, 0u, code) == 0u) {
+        g_error.site = site;
+        g_error.cta = blockIdx.x;
+        g_error.info = info;
+        __threadfence();
+    }
+}
+
+__device__ __forceinline__ bool aborted(const WaitCtx& w) {
+    return w.abort != nullptr && ld_relaxed_u32(w.abort) == w.abort_val;
+}
+
+__device__ __forceinline__ void raise_abort(const WaitCtx& w) {
+    if (w.abort != nullptr) st_relaxed_u32(const_cast<uint32_t*>(w.abort), w.abort_val);
+}
+
+// Bounded wait on an mbarrier phase.  False: timed out (recorded) or the call
+// was aborted elsewhere.
+__device__ __forceinline__ bool wait_mbar(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t n = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++n & 63u) == 0u) {
+            if (aborted(w)) return false;
+            if ((long long)(globaltimer() - t0) > w.limit_ns) {
+                record_error(ERR_TIMEOUT, site, parity);
+                raise_abort(w);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// Bounded wait for *p >= target (acquire).
+__device__ __forceinline__ bool wait_geq(const uint32_t* p, uint32_t target, const WaitCtx& w, int site) {
+    if (ld_acquire_u32(p) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t n = 0;
+    while (ld_acquire_u32(p) < target) {
+        __nanosleep(64);
+        if ((++n & 15u) == 0u) {
+            if (aborted(w)) return false;
+            if ((long long)(globaltimer() - t0) > w.limit_ns) {
+                record_error(ERR_TIMEOUT, site, target);
+                raise_abort(w);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// Bounded wait for *p == v (acquire).
+__device__ __forceinline__ bool wait_eq(const uint32_t* p, uint32_t v, const WaitCtx& w, int site) {
+    if (ld_acquire_u32(p) == v) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t n = 0;
+    while (ld_acquire_u32(p) != v) {
+        __nanosleep(32);
+        if ((++n & 15u) == 0u) {
+            if (aborted(w)) return false;
+            if ((long long)(globaltimer() - t0) > w.limit_ns) {
+                record_error(ERR_TIMEOUT, site, v);
+                raise_abort(w);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void stamp(const Params& p, int slot) {
+    if (p.trace && threadIdx.x == 0) p.trace_buf[blockIdx.x * TRACE_SLOTS + slot] = globaltimer();
+}
+
+// ------------------------------------------------------ shared control -----
+
+struct Info {
+    int e, row0, nrows, nbk;
+};
+
+struct CtrlSmem {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t info_full[4];
+    uint64_t info_empty[4];
+    uint64_t drain;
+    uint64_t gbar[MAX_GATHER_SLOTS];
+    Info info[4];
+    uint32_t tmem_base;
+    int32_t bcast[8];
+    int32_t offs[MAX_E + 1];
+    int32_t tile_start[MAX_E + 1];
+    int32_t item_start[MAX_E + 1];
+    int32_t tot[MAX_E];
+};
+static_assert(sizeof(CtrlSmem) <= SM_CTRL_BYTES, "control smem too large");
+
+__device__ __forceinline__ uint8_t* smem_base() {
+    extern __shared__ uint8_t smem_raw[];
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ CtrlSmem* ctrl() { return reinterpret_cast<CtrlSmem*>(smem_base() + SM_CTRL); }
+
+// ------------------------------------------------------------ phase R ------
+
+// Key order of the router: (value desc, expert id asc).
+__device__ __forceinline__ bool beats(float v, int e, float u, int f) { return v > u || (v == u && e < f); }
+
+// Route one chunk of ROUTE_CHUNK tokens: top-k + gates, per-chunk histogram,
+// and each (t, j)'s rank among the chunk's entries of the same expert in
+// (t, j) order.  Whole CTA.
+__device__ void route_chunk(const Params& p, int c) {
+    uint8_t* s = smem_base();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* slog = reinterpret_cast<float*>(s + RT_LOGITS) + warp * 32 * RT_LOGIT_STRIDE;
+    int* sidx = reinterpret_cast<int*>(s + RT_IDX) + warp * 32 * MAX_K;
+    int* slr = reinterpret_cast<int*>(s + RT_LRANK) + warp * 32 * MAX_K;
+    int* wcnt = reinterpret_cast<int*>(s + RT_WCNT);
+    const int E = p.E, k = p.k, T = p.T;
+    const int tbase = c * ROUTE_CHUNK + warp * 32;
+    const int t = tbase + lane;
+
+    for (int e = lane; e < E; e += 32) wcnt[warp * MAX_E + e] = 0;
+
+    float vals[MAX_K];
+    int ids[MAX_K];
+#pragma unroll
+    for (int j = 0; j < MAX_K; ++j) {
+        vals[j] = -INFINITY;
+        ids[j] = 0x7fffffff;
+    }
+    for (int e0 = 0; e0 < E; e0 += 64) {
+        const int ne = min(64, E - e0);
+        __syncwarp();
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+            const int ti = tbase + i;
+            if (ti < T) {
+                const float* row = p.logits + size_t(ti) * E + e0;
+                if (lane < ne) slog[i * RT_LOGIT_STRIDE + lane] = __ldg(row + lane);
+                if (lane + 32 < ne) slog[i * RT_LOGIT_STRIDE + lane + 32] = __ldg(row + lane + 32);
+            }
+        }
+        __syncwarp();
+        if (t < T) {
+            for (int ee = 0; ee < ne; ++ee) {
+                const float v = slog[lane * RT_LOGIT_STRIDE + ee];
+                const int e = e0 + ee;
+                if (beats(v, e, vals[MAX_K - 1], ids[MAX_K - 1])) {
+                    // sorted insertion of (v, e) into the 8-entry list
+                    bool b[MAX_K];
+#pragma unroll
+                    for (int j = 0; j < MAX_K; ++j) b[j] = beats(v, e, vals[j], ids[j]);
+#pragma unroll
+                    for (int j = MAX_K - 1; j >= 0; --j) {
+                        if (b[j]) {
+                            const bool prev = (j > 0) && b[j - 1];
+                            vals[j] = prev ? vals[j - 1] : v;
+                            ids[j] = prev ? ids[j - 1] : e;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    if (t < T) {
+        // ids outside [0, E) only survive for NaN rows (outside the contract)
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) ids[j] = min(max(ids[j], 0), E - 1);
+        const float l0 = vals[0];
+        float g[MAX_K];
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
+            g[j] = 0.f;
+            if (j < k && l0 != -INFINITY) {
+                g[j] = expf(vals[j] - l0);
+                sum += g[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
+            if (j < k) {
+                const float gj = (l0 == -INFINITY) ? 0.f : g[j] / sum;
+                p.topk_idx[size_t(t) * k + j] = ids[j];
+                p.topk_gate[size_t(t) * k + j] = gj;
+                sidx[lane * MAX_K + j] = ids[j];
+            }
+        }
+    }
+    __syncwarp();
+
+    // In-warp stable ranks: lanes hold (token, slot) entries in (t, j) order,
+    // 32/k tokens per pass; equal experts are found with match.any.
+    const int G = 32 / k;
+    const uint32_t lt = lanemask_lt();
+    for (int it = 0; it * G < 32; ++it) {
+        const int g = lane / k, j = lane - (lane / k) * k;
+        const int tok = it * G + g;
+        const bool valid = (lane < G * k) && (tok < 32) && (tbase + tok < T);
+        const int e = valid ? sidx[tok * MAX_K + j] : -(lane + 1);
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        const int before = __popc(peers & lt);
+        const int base = valid ? wcnt[warp * MAX_E + e] : 0;
+        __syncwarp();
+        if (valid && before == 0) wcnt[warp * MAX_E + e] = base + __popc(peers);
+        __syncwarp();
+        if (valid) slr[tok * MAX_K + j] = base + before;
+    }
+    __syncthreads();
+
+    // Chunk counts and per-warp exclusive bases.
+    for (int e = threadIdx.x; e < E; e += NTHREADS) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) {
+            const int v = wcnt[w * MAX_E + e];
+            wcnt[w * MAX_E + e] = run;
+            run += v;
+        }
+        p.counts[size_t(c) * E + e] = run;
+    }
+    __syncthreads();
+    if (t < T) {
+        for (int j = 0; j < k; ++j) {
+            const int e = sidx[lane * MAX_K + j];
+            p.lrank[size_t(t) * k + j] = slr[lane * MAX_K + j] + wcnt[warp * MAX_E + e];
+        }
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------ phase S ------
+
+// Exclusive scans of per-expert totals into offsets, tile starts and item
+// starts (warp 0; E <= 256, 8 experts per lane).
+__device__ void build_tables(const Params& p, CtrlSmem* cs) {
+    if ((threadIdx.x >> 5) != 0) return;
+    const int lane = threadIdx.x & 31;
+    const int E = p.E;
+    int lo[8], lt[8], li[8];
+    int so = 0, st = 0, si = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        const int v = (e < E) ? cs->tot[e] : 0;
+        const int nt = (v + BM - 1) / BM;
+        lo[i] = so;
+        lt[i] = st;
+        li[i] = si;
+        so += v;
+        st += nt;
+        si += nt * p.nb;
+    }
+    int io = so, it = st, ii = si;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, io, o);
+        const int b = __shfl_up_sync(0xffffffffu, it, o);
+        const int c = __shfl_up_sync(0xffffffffu, ii, o);
+        if (lane >= o) {
+            io += a;
+            it += b;
+            ii += c;
+        }
+    }
+    const int eo = io - so, et = it - st, ei = ii - si;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        if (e < E) {
+            cs->offs[e] = eo + lo[i];
+            cs->tile_start[e] = et + lt[i];
+            cs->item_start[e] = ei + li[i];
+        }
+    }
+    if (lane == 31) {
+        cs->offs[E] = io;
+        cs->tile_start[E] = it;
+        cs->item_start[E] = ii;
+    }
+}
+
+// Totals from the full counts table; for the CTA's own chunks, the column
+// prefix (rows of earlier chunks) is kept in smem as the chunk's bases.
+__device__ void scan_counts(const Params& p, CtrlSmem* cs, bool keep_bases) {
+    int* sbase = reinterpret_cast<int*>(smem_base() + RT_BASES);
+    const int E = p.E, nch = p.nch, grid = gridDim.x;
+    for (int e = threadIdx.x; e < E; e += NTHREADS) {
+        int run = 0, m = 0;
+        int mine = blockIdx.x;
+        for (int c = 0; c < nch; ++c) {
+            if (keep_bases && c == mine) {
+                sbase[m * MAX_E + e] = run;
+                ++m;
+                mine += grid;
+            }
+            run += __ldcg(p.counts + size_t(c) * E + e);
+        }
+        cs->tot[e] = run;
+    }
+    __syncthreads();
+    build_tables(p, cs);
+    __syncthreads();
+    if (keep_bases) {
+        int m = 0;
+        for (int c = blockIdx.x; c < nch; c += grid, ++m)
+            for (int e = threadIdx.x; e < E; e += NTHREADS) sbase[m * MAX_E + e] += cs->offs[e];
+    }
+    __syncthreads();
+}
+
+// Scatter src_index / gate_w for (t, j) entries of chunk c (bases in smem).
+__device__ void scatter_chunk(const Params& p, int c, const int* cbase, const WaitCtx& w) {
+    const int k = p.k, T = p.T;
+    const int t0 = c * ROUTE_CHUNK;
+    const int n = min(ROUTE_CHUNK, T - t0) * k;
+    for (int i = threadIdx.x; i < n; i += NTHREADS) {
+        const int q = t0 * k + i;
+        const int e = __ldcg(p.topk_idx + q);
+        const int dest = cbase[e] + __ldcg(p.lrank + q);
+        if (dest < 0 || dest >= p.rows) {
+            record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(dest));
+            raise_abort(w);
+            continue;
+        }
+        p.src_index[dest] = q;
+        p.gate_w[dest] = __ldcg(p.topk_gate + q);
+    }
+}
+
+// ------------------------------------------------------------- gather ------
+
+__device__ __forceinline__ int find_expert(const int32_t* starts, int E, int v) {
+    // largest e with starts[e] <= v (starts[0] = 0 <= v < starts[E])
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (starts[mid] <= v) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Dispatch role: pull tiles (GEMM consumption order) from the gather queue;
+// each of `gather_slots` lanes of warp 0 moves one row at a time
+// x[src] -> smem -> xs[row] with bulk copies; the tile's flag is released
+// once all its rows are written.
+__device__ void gather_role(const Params& p, CtrlSmem* cs, uint32_t flag, const WaitCtx& w) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp != 0) return;
+    uint8_t* s = smem_base();
+    const uint32_t row_bytes = uint32_t(p.H) * 2u;
+    const int nslot = p.gather_slots;
+    const int ntiles = cs->tile_start[p.E];
+    uint32_t ph = 0;
+    bool ok = true;
+    while (ok) {
+        int tile = 0;
+        if (lane == 0) tile = int(atom_add_relaxed_u32(&p.ctl->next_tile, 1u));
+        tile = __shfl_sync(0xffffffffu, tile, 0);
+        if (tile >= ntiles) break;
+        const int e = find_expert(cs->tile_start, p.E, tile);
+        const int row0 = cs->offs[e] + (tile - cs->tile_start[e]) * BM;
+        const int nrows = min(BM, cs->offs[e + 1] - row0);
+        if (lane < nslot) {
+            uint8_t* slot = s + size_t(lane) * row_bytes;
+            for (int i = lane; i < nrows && ok; i += nslot) {
+                const int r = row0 + i;
+                const int src_t = __ldcg(p.src_index + r) / p.k;
+                if (src_t < 0 || src_t >= p.T) {
+                    record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(r));
+                    raise_abort(w);
+                    ok = false;
+                    break;
+                }
+                bulk_wait_read<0>();
+                mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
+                bulk_load(slot, p.x + size_t(src_t) * p.H, row_bytes, &cs->gbar[lane]);
+                if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
+                    ok = false;
+                    // the load is in flight: give it a short, bounded chance to land
+                    WaitCtx shortw{nullptr, 0u, 2000000LL};
+                    wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
+                }
+                ph ^= 1u;
+                if (ok) {
+                    bulk_store(p.xs + size_t(r) * p.H, slot, row_bytes);
+                    bulk_commit();
+                }
+            }
+            bulk_wait_all();
+            fence_proxy_async();
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0 && ok && tile != p.debug_drop_tile) {
+            __threadfence();
+            st_release_u32(p.ready + tile, flag);
+        }
+        if (aborted(w)) break;
+    }
+    bulk_wait_all();
+}
+
+// Unfused path: push-gather of chunk c (every entry to its destination row).
+__device__ void push_gather_chunk(const Params& p, int c, CtrlSmem* cs, uint32_t& ph, const WaitCtx& w) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp != 0) return;
+    uint8_t* s = smem_base();
+    const uint32_t row_bytes = uint32_t(p.H) * 2u;
+    const int nslot = p.gather_slots;
+    const int k = p.k, T = p.T;
+    const int t0 = c * ROUTE_CHUNK;
+    const int n = min(ROUTE_CHUNK, T - t0) * k;
+    if (lane < nslot) {
+        uint8_t* slot = s + size_t(lane) * row_bytes;
+        for (int i = lane; i < n; i += nslot) {
+            const int q = t0 * k + i;
+            const int e = __ldcg(p.topk_idx + q);
+            const int dest = __ldcg(p.bases + size_t(c) * p.E + e) + __ldcg(p.lrank + q);
+            if (dest < 0 || dest >= p.rows) {
+                record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(dest));
+                continue;
+            }
+            p.src_index[dest] = q;
+            p.gate_w[dest] = __ldcg(p.topk_gate + q);
+            bulk_wait_read<0>();
+            mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
+            bulk_load(slot, p.x + size_t(q / k) * p.H, row_bytes, &cs->gbar[lane]);
+            if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
+                WaitCtx shortw{nullptr, 0u, 2000000LL};
+                wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
+                ph ^= 1u;
+                break;
+            }
+            ph ^= 1u;
+            bulk_store(p.xs + size_t(dest) * p.H, slot, row_bytes);
+            bulk_commit();
+        }
+        bulk_wait_all();
+    }
+}
+
+// ------------------------------------------------------------ compute ------
+
+__device__ __forceinline__ void decode_item(const Params& p, const CtrlSmem* cs, int item, Info& inf, int& gtile) {
+    const int e = find_expert(cs->item_start, p.E, item);
+    const int local = item - cs->item_start[e];
+    const int nt = cs->tile_start[e + 1] - cs->tile_start[e];
+    const int NB = p.nb, G = p.n_group;
+    const int full = NB / G;
+    int t_in, nbk;
+    if (local < full * nt * G) {
+        const int g = local / (nt * G);
+        const int r = local - g * (nt * G);
+        t_in = r / G;
+        nbk = g * G + (r - t_in * G);
+    } else {
+        const int l2 = local - full * nt * G;
+        const int Gl = NB - full * G;
+        t_in = l2 / Gl;
+        nbk = full * G + (l2 - t_in * Gl);
+    }
+    inf.e = e;
+    inf.row0 = cs->offs[e] + t_in * BM;
+    inf.nrows = min(BM, cs->offs[e + 1] - inf.row0);
+    inf.nbk = nbk;
+    gtile = cs->tile_start[e] + t_in;
+}
+
+constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+
+// Warp-specialised expert GEMM over work items (tile, N-block) taken from the
+// shared queue until it is empty.  wait_ready: spin on the tile's flag first.
+__device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, CtrlSmem* cs,
+                             bool wait_ready, uint32_t flag, const WaitCtx& w) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* s = smem_base();
+    const int total_items = cs->item_start[p.E];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_par = 0, issued_any = 0;  // per-stage bit: parity of the last issue
+            bool ok = true;
+            uint32_t next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+            for (uint32_t it = 0; ok; ++it) {
+                const int item = int(next);
+                const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+                if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, w, SITE_INFO_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                if (item >= total_items) {
+                    cs->info[slot].e = -1;
+                    mbar_arrive(&cs->info_full[slot]);
+                    break;
+                }
+                next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);  // prefetch the next item
+                Info inf;
+                int gtile;
+                decode_item(p, cs, item, inf, gtile);
+                cs->info[slot] = inf;
+                mbar_arrive(&cs->info_full[slot]);
+                if (wait_ready) {
+                    if (!wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async();
+                }
+                const int ncol = p.F;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!wait_mbar(&cs->empty[stage], phase ^ 1u, w, SITE_STAGE_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    uint64_t* fb = &cs->full[stage];
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
+                    uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
+                    tma_load_2d(a, tmA, kb * BK, inf.row0, fb);
+#pragma unroll
+                    for (int q = 0; q < BN / 64; ++q) {
+                        const int col = inf.nbk * BN + q * 64;
+                        // chunks past F read as zeros (out of bounds fill)
+                        tma_load_2d(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK, fb);
+                    }
+                    issued_any |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every issued tensor load land before the CTA can exit
+                WaitCtx shortw{nullptr, 0u, 5000000LL};
+                for (int st = 0; st < STAGES; ++st)
+                    if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
+            bool issued = false;
+            for (uint32_t it = 0;; ++it) {
+                const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+                if (!wait_mbar(&cs->info_full[slot], iph, w, SITE_INFO_FULL)) break;
+                const int e = cs->info[slot].e;
+                mbar_arrive(&cs->info_empty[slot]);
+                if (e < 0) break;
+                if (!wait_mbar(&cs->acc_empty[acc], accph ^ 1u, w, SITE_ACC_EMPTY)) break;
+                tc_fence_after();
+                const uint32_t d = cs->tmem_base + acc * BN;
+                bool ok = true;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!wait_mbar(&cs->full[stage], phase, w, SITE_STAGE_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(s + SM_A + stage * A_STAGE_BYTES);
+                    const uint32_t b0 = smem_u32(s + SM_B + stage * B_STAGE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // A: K-major, 128B swizzle, 8-row groups 1024 B apart; +32 B per K=16
+                        const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
+                        // B: N-major, 128B swizzle; 64-column chunks 8 KiB apart (LBO),
+                        // 8-row K groups 1024 B apart (SBO); +2 KiB per K=16
+                        const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
+                        tc_mma_f16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit(&cs->empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&cs->acc_full[acc]);
+                acc ^= 1u;
+                if (acc == 0) accph ^= 1u;
+            }
+            if (issued) {
+                // every MMA this thread issued has completed before TMEM is freed
+                tc_commit(&cs->drain);
+                WaitCtx shortw{nullptr, 0u, 5000000LL};
+                wait_mbar(&cs->drain, 0u, shortw, SITE_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warps 2..5 ----------------
+        const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32)
+        uint32_t acc = 0, accph = 0;
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+            if (!wait_mbar(&cs->info_full[slot], iph, w, SITE_INFO_FULL)) break;
+            const Info inf = cs->info[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cs->info_empty[slot]);
+            if (inf.e < 0) break;
+            if (!wait_mbar(&cs->acc_full[acc], accph, w, SITE_ACC_FULL)) break;
+            tc_fence_after();
+            const int rloc = quad * 32 + lane;
+            const bool rowok = rloc < inf.nrows;
+            const size_t row = size_t(inf.row0) + rloc;
+            const int n0 = inf.nbk * BN;
+            const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                const int col = n0 + cc * 32;
+                if (col >= p.F) break;
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                tmem_ld_wait();
+                if (rowok) {
+                    if (p.out_f32) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.y) + row * p.F + col);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + row * p.F + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * u]),
+                                                                               __uint_as_float(r[8 * v + 2 * u + 1]));
+                                pk[u] = *reinterpret_cast<const uint32_t*>(&h);
+                            }
+                            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&cs->acc_empty[acc]);
+            acc ^= 1u;
+            if (acc == 0) accph ^= 1u;
+        }
+    }
+}
+
+// ----------------------------------------------------------- CTA setup -----
+
+__device__ void cta_setup(CtrlSmem* cs, bool with_tmem) {
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&cs->full[i], 1);
+            mbar_init(&cs->empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&cs->acc_full[i], 1);
+            mbar_init(&cs->acc_empty[i], 128);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&cs->info_full[i], 1);
+            mbar_init(&cs->info_empty[i], 1 + 4);
+        }
+        mbar_init(&cs->drain, 1);
+        for (int i = 0; i < MAX_GATHER_SLOTS; ++i) mbar_init(&cs->gbar[i], 1);
+        fence_barrier_init();
+    }
+    if (with_tmem && warp == 1) {
+        tmem_alloc(&cs->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+__device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
+    tc_fence_before();
+    __syncthreads();
+    if (with_tmem && (threadIdx.x >> 5) == 1) {
+        tc_fence_after();
+        tmem_dealloc(cs->tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0) {
+        if (p.trace) p.trace_buf[blockIdx.x * TRACE_SLOTS + 15] = globaltimer();
+        const uint32_t old = atom_add_acq_rel_u32(&p.ctl->exit_count, 1u);
+        if (old == gridDim.x - 1) {
+            // last CTA out: leave the control block ready for the next call
+            Ctl* c = p.ctl;
+            c->bar_routed = 0;
+            c->bar_scattered = 0;
+            c->next_tile = 0;
+            c->next_item = 0;
+            c->items_done = 0;
+            c->abort = 0;
+            c->epoch = c->epoch + 1u;  // calls completed on this workspace
+            c->exit_count = 0;
+            __threadfence();
+        }
+    }
+}
+
+// ------------------------------------------------------------- kernels -----
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    mk_fused_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    CtrlSmem* cs = ctrl();
+    const uint32_t flag = 1u;  // tile ready / call aborted
+    const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
+    const bool is_dispatch = int(blockIdx.x) < p.dispatch_ctas;
+    stamp(p, 0);
+    if (threadIdx.x == 0 && p.compute) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    cta_setup(cs, p.compute != 0);
+
+    // This call's readiness flags start at 0.  Cleared before the routing
+    // barrier; they are set only after it, so no stale value is ever seen.
+    for (int i = blockIdx.x * NTHREADS + threadIdx.x; i < p.max_tiles; i += gridDim.x * NTHREADS) p.ready[i] = 0u;
+
+    // phase R
+    for (int c = blockIdx.x; c < p.nch; c += gridDim.x) route_chunk(p, c);
+    stamp(p, 1);
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atom_add_acq_rel_u32(&p.ctl->bar_routed, 1u);
+        ok = wait_geq(&p.ctl->bar_routed, gridDim.x, w, SITE_BAR_ROUTED);
+        cs->bcast[0] = ok;
+    }
+    __syncthreads();
+    ok = cs->bcast[0] != 0;
+    stamp(p, 2);
+
+    if (ok) {
+        // phase S
+        scan_counts(p, cs, true);
+        if (blockIdx.x == 0)
+            for (int e = threadIdx.x; e <= p.E; e += NTHREADS) p.expert_offsets[e] = cs->offs[e];
+        if (threadIdx.x == 0 && cs->offs[p.E] != p.rows) {
+            record_error(ERR_FAULT, SITE_ROW_TOTAL, uint32_t(cs->offs[p.E]));
+            raise_abort(w);
+        }
+        const int* sbase = reinterpret_cast<const int*>(smem_base() + RT_BASES);
+        int m = 0;
+        for (int c = blockIdx.x; c < p.nch; c += gridDim.x, ++m) scatter_chunk(p, c, sbase + m * MAX_E, w);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atom_add_acq_rel_u32(&p.ctl->bar_scattered, 1u);
+        }
+        stamp(p, 3);
+
+        if (is_dispatch) {
+            if (threadIdx.x == 0) cs->bcast[1] = wait_geq(&p.ctl->bar_scattered, gridDim.x, w, SITE_BAR_SCATTERED);
+            fence_proxy_async_shared();  // generic smem use (routing) before bulk copies into it
+            __syncthreads();
+            stamp(p, 4);
+            if (cs->bcast[1]) gather_role(p, cs, flag, w);
+            __syncthreads();
+            stamp(p, 5);
+        }
+        if (threadIdx.x == 0) cs->bcast[2] = p.compute && !aborted(w);
+        fence_proxy_async_shared();  // generic/bulk smem use before TMA writes into it
+        __syncthreads();
+        if (cs->bcast[2]) {
+            stamp(p, 6);
+            compute_role(p, &tmA, &tmB, cs, true, flag, w);
+            stamp(p, 7);
+        }
+    }
+    cta_teardown(p, cs, p.compute != 0);
+}
+
+// Unfused baseline, launch 1: routing per chunk.
+__global__ void __launch_bounds__(NTHREADS, 1) mk_route_kernel(const Params p) {
+    route_chunk(p, blockIdx.x);
+}
+
+// Unfused baseline, launch 2: offsets and per-chunk bases (one CTA).
+__global__ void __launch_bounds__(NTHREADS, 1) mk_scan_kernel(const Params p) {
+    CtrlSmem* cs = ctrl();
+    const int E = p.E;
+    for (int e = threadIdx.x; e < E; e += NTHREADS) {
+        int run = 0;
+        for (int c = 0; c < p.nch; ++c) run += p.counts[size_t(c) * E + e];
+        cs->tot[e] = run;
+    }
+    __syncthreads();
+    build_tables(p, cs);
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += NTHREADS) p.expert_offsets[e] = cs->offs[e];
+    for (int e = threadIdx.x; e < E; e += NTHREADS) {
+        int run = cs->offs[e];
+        for (int c = 0; c < p.nch; ++c) {
+            const int v = p.counts[size_t(c) * E + e];
+            p.bases[size_t(c) * E + e] = run;
+            run += v;
+        }
+    }
+}
+
+// Unfused baseline, launch 3: scatter + push-gather per chunk.
+__global__ void __launch_bounds__(NTHREADS, 1) mk_gather_kernel(const Params p) {
+    CtrlSmem* cs = ctrl();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < MAX_GATHER_SLOTS; ++i) mbar_init(&cs->gbar[i], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const WaitCtx w{nullptr, 0u, p.spin_limit_ns};
+    uint32_t ph = 0;
+    push_gather_chunk(p, blockIdx.x, cs, ph, w);
+}
+
+// Unfused baseline, launch 4: persistent expert GEMM over all tiles.
+__global__ void __launch_bounds__(NTHREADS, 1)
+    mk_gemm_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    CtrlSmem* cs = ctrl();
+    const uint32_t flag = 1u;
+    const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    cta_setup(cs, true);
+    for (int e = threadIdx.x; e < p.E; e += NTHREADS) cs->tot[e] = p.expert_offsets[e + 1] - p.expert_offsets[e];
+    __syncthreads();
+    build_tables(p, cs);
+    __syncthreads();
+    compute_role(p, &tmA, &tmB, cs, false, flag, w);
+    cta_teardown(p, cs, true);
+}
+
+// ---------------------------------------------------------- host hooks -----
+
+cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (they wait on each other)
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mk_fused_kernel, p, a, b);
+}
+
+cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st) {
+    mk_route_kernel<<<p.nch, NTHREADS, SMEM_BYTES, st>>>(p);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    mk_scan_kernel<<<1, NTHREADS, SMEM_BYTES, st>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    mk_gather_kernel<<<p.nch, NTHREADS, SMEM_BYTES, st>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    mk_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b);
+    return cudaGetLastError();
+}
+
+cudaError_t set_kernel_attributes() {
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(mk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+        return err;
+    if ((err = cudaFuncSetAttribute(mk_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+        return err;
+    if ((err = cudaFuncSetAttribute(mk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+        return err;
+    if ((err = cudaFuncSetAttribute(mk_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+        return err;
+    return cudaFuncSetAttribute(mk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+}
+
+cudaError_t fused_max_blocks_per_sm(int* n) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, mk_fused_kernel, NTHREADS, SMEM_BYTES);
+}
+
+cudaError_t read_and_clear_error(uint32_t out[4], cudaStream_t st) {
+    DevError e{};
+    cudaError_t err = cudaMemcpyFromSymbolAsync(&e, g_error, sizeof(e), 0, cudaMemcpyDeviceToHost, st);
+    if (err != cudaSuccess) return err;
+    if ((err = cudaStreamSynchronize(st)) != cudaSuccess) return err;
+    out[0] = e.code;
+    out[1] = e.site;
+    out[2] = e.cta;
+    out[3] = e.info;
+    if (e.code != 0) {
+        DevError z{};
+        if ((err = cudaMemcpyToSymbolAsync(g_error, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st))) return err;
+        err = cudaStreamSynchronize(st);
+    }
+    return err;
+}
+
+}  // namespace mk

@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MoE dispatch + expert GEMM on GB300.
+
+One step = one pass of the whole path (router top-k, histogram + scan,
+gather into expert-contiguous tiles, expert GEMM) over one batch of the
+seeded synthetic workload, through the C ABI.  Default workload: the
+Mixtral-like layer (T=4096, H=4096, F=14336, E=8, top-2, seed 1).
+
+Timing: W warm-up steps, then K timed steps; every step is bracketed by CUDA
+events on the launching stream, with a 256 MiB write (larger than L2)
+between steps outside the events; the timed region is bracketed by a
+barrier and a device synchronise; the max over ranks is taken.  Under
+torchrun every rank runs its own batch (weak scaling, no data-path
+collective).
+
+``--impl reference`` times the CPU oracle instead (rank 0 only).
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from moe_token_dispatch_persistent_gb300 import synth  # noqa: E402
+
+METRIC = "fused dispatch+grouped-GEMM TFLOP/s (% bf16 peak) and dispatch GB/s (% HBM)"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--dispatch-ctas", type=int, default=0)
+    ap.add_argument("--n-group", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true", help="skip unfused / dispatch-only / e2e / cpu legs")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------- helpers --
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w: synth.Workload, extra=None):
+    c = {"workload": w.describe(), "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k, "seed": w.seed,
+         "l2": "flushed between timed steps (256 MiB write, outside the events)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over ranks (identity at world 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank: float, world: int, seconds_max: float) -> float:
+    return flop_per_rank * world / seconds_max / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                n += 1
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ------------------------------------------------------------ reference --
+
+_WE_CACHE = {}
+
+
+def oracle_sample(w: synth.Workload, budget_s: float, inputs=None):
+    """Time the CPU oracle on a bounded sample of workload ``w``.
+
+    The full routing + dispatch of all T tokens is timed once; the fp64
+    expert product is timed on a sample of sorted rows sized to the budget.
+    The full-workload time is estimated as t_routing + t_row * T*k, and the
+    value is the workload's FLOPs over that estimate.
+    """
+    from oracle.oracle import Oracle
+
+    orc = Oracle()
+    if inputs is None:
+        ch = synth._streams(w)
+        logits = synth.make_logits(w, ch)
+        x = synth.make_x(w, ch)
+    else:
+        x, logits = inputs
+    t0 = time.perf_counter()
+    idx, gate = orc.route(logits, w.k)
+    offsets, src, gw = orc.dispatch(idx, gate, w.E)
+    t_route = time.perf_counter() - t0
+    # rows of the most loaded expert: one weight matrix for the whole sample
+    e = int(np.argmax(np.diff(offsets)))
+    key = (w.seed, w.E, w.H, w.F, e)
+    if key not in _WE_CACHE:
+        _WE_CACHE.clear()
+        _WE_CACHE[key] = synth.make_w_expert(w, e)
+    We = _WE_CACHE[key]
+    off1 = np.array([0, offsets[e + 1] - offsets[e]], dtype=np.int32)
+    src1 = src[offsets[e]:offsets[e + 1]]
+    n = max(1, min(off1[1], orc.num_threads()))
+    t0 = time.perf_counter()
+    orc.expert_rows(x, We[None], w.k, off1, src1, np.arange(n))
+    t_cal = (time.perf_counter() - t0) / n
+    n = int(max(1, min(off1[1], budget_s / max(t_cal, 1e-9))))
+    t0 = time.perf_counter()
+    orc.expert_rows(x, We[None], w.k, off1, src1, np.arange(n))
+    t_rows = time.perf_counter() - t0
+    t_row = t_rows / n
+    est = t_route + t_row * w.rows
+    return {
+        "value": w.flop / est / 1e12,
+        "unit": UNIT,
+        "cores": orc.num_threads(),
+        "kind": "oracle",
+        "sample": (f"routing+dispatch of all {w.T} tokens ({t_route:.3f} s) + fp64 product of {n} sorted rows "
+                   f"({t_rows:.2f} s); full-workload time estimated as t_route + t_row*{w.rows} = {est:.1f} s"),
+        "seconds_estimated_full": est,
+    }
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    per_step_budget = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    times, cb = [], None
+    ch = synth._streams(w)
+    inputs = (synth.make_x(w, ch), synth.make_logits(w, ch))
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(w, per_step_budget, inputs)
+        if i >= args.warmup:
+            times.append(r["seconds_estimated_full"])
+            cb = r
+    est = statistics.mean(times)
+    value = w.flop / est / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": workload_config(w, {"l2": "n/a (CPU)"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ ours --
+
+def dispatch_bytes(w: synth.Workload) -> int:
+    """Algorithmic bytes of the dispatch role: logits read, token rows read and
+    written to the staging tiles, src_index / gate_w written, offsets."""
+    return w.T * w.E * 4 + 2 * w.rows * w.H * 2 + w.rows * 8 + (w.E + 1) * 4
+
+
+def compulsory_bytes(w: synth.Workload, active_experts: int) -> int:
+    """x + logits + active experts' W + y_sorted (bf16) + src_index + gate_w + offsets."""
+    return (w.T * w.H * 2 + w.T * w.E * 4 + active_experts * w.H * w.F * 2 + w.rows * w.F * 2 + w.rows * 8
+            + (w.E + 1) * 4)
+
+
+def run_ours(args, w):
+    import torch
+
+    import moe_token_dispatch_persistent_gb300 as mk
+    from moe_token_dispatch_persistent_gb300 import build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peaks_src = load_peaks()
+
+    # inputs: each rank its own batch of tokens (seed offset), same expert weights
+    wr = synth.Workload(w.name, w.T, w.H, w.F, w.E, w.k, w.seed + 1000 * rank, w.kind) if rank else w
+    ch = synth._streams(wr)
+    x_np, l_np = synth.make_x(wr, ch), synth.make_logits(wr, ch)
+    W_np = synth.make_w(w)
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    logits = torch.from_numpy(l_np).to(dev)
+    W = torch.from_numpy(W_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    del W_np
+    out = mk.alloc_outputs(w.T, w.F, w.E, w.k, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cfg = mk.make_config(dispatch_ctas=args.dispatch_ctas, n_group=args.n_group)
+
+    def call(c):
+        st = mk.mk_moe_dispatch_gemm_ex(x, logits, w.T, w.H, w.E, w.k, W, w.F, out["y_sorted"], out["src_index"],
+                                        out["expert_offsets"], out["gate_w"], stream, c)
+        if st != mk.MK_OK:
+            raise mk.MkError(st, "mk_moe_dispatch_gemm_ex")
+
+    def timed(c, steps, warmup):
+        for _ in range(warmup):
+            flush.fill_(1)
+            call(c)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            call(c)
+            b.record(stream)
+        torch.cuda.synchronize()
+        st = mk.mk_get_status(stream)
+        if st != mk.MK_OK:
+            raise mk.MkError(st, "device status")
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # headline: fused path
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call(cfg)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    launches_before = 0
+    ms = timed(cfg, args.steps, 0)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    info = mk.mk_last_launch_info()
+    gpu_launches = args.steps * info["launches"] + launches_before
+    ms_mean = statistics.mean(ms)
+    ms_max = reduce_max(ms_mean, world)
+    value = whole_job_tflops(w.flop, world, ms_max / 1e3)
+    offs = out["expert_offsets"].cpu().numpy()
+    active = int((np.diff(offs) > 0).sum())
+
+    achieved = w.flop / (ms_mean / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, {"mode": "fused persistent", "grid_ctas": info["grid_ctas"],
+                                      "dispatch_ctas": info["dispatch_ctas"], "n_group": info["n_group"],
+                                      "active_experts": active}),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"bf16_tflops (burst), {peaks_src}",
+                     "kernel": "mk_fused_kernel", "traffic": None,
+                     "compulsory_bytes": compulsory_bytes(w, active)},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "ms_per_step_min": min(ms), "ms_per_step_median": statistics.median(ms),
+    }
+
+    if not args.no_extras:
+        # dispatch role alone (routing + gather), GB/s against HBM
+        dcfg = mk.make_config(mode=mk.MK_MODE_DISPATCH_ONLY)
+        dms = statistics.mean(timed(dcfg, min(args.steps, 50), 3))
+        db = dispatch_bytes(w)
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        line["dispatch"] = {"gbs": db / (dms / 1e3) / 1e9, "frac_hbm": db / (dms / 1e3) / 1e9 / hbm,
+                            "ms": dms, "bytes": db, "peak_gbs": hbm}
+        # the same steps as four launches (host-driven baseline)
+        ucfg = mk.make_config(mode=mk.MK_MODE_UNFUSED)
+        ums = statistics.mean(timed(ucfg, min(args.steps, 50), 3))
+        line["unfused"] = {"ms_per_step": ums, "tflops": w.flop / (ums / 1e3) / 1e12,
+                           "fused_speedup": ums / ms_mean, "launches_per_step": 4}
+        # end to end through the host-buffer entry point
+        xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+        lh = torch.from_numpy(l_np).pin_memory()
+        yh = torch.empty((w.rows, w.F), dtype=torch.int16).pin_memory()
+        sh = torch.empty(w.rows, dtype=torch.int32).pin_memory()
+        oh = torch.empty(w.E + 1, dtype=torch.int32).pin_memory()
+        gh = torch.empty(w.rows, dtype=torch.float32).pin_memory()
+        e2e_steps = max(3, min(args.steps, 30))
+        et = []
+        for i in range(args.warmup + e2e_steps):
+            flush.fill_(1)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            st = mk.mk_moe_dispatch_gemm_host(xh, lh, w.T, w.H, w.E, w.k, W, w.F, yh, sh, oh, gh, stream, cfg)
+            t1 = time.perf_counter()
+            if st != mk.MK_OK:
+                raise mk.MkError(st, "mk_moe_dispatch_gemm_host")
+            if i >= args.warmup:
+                et.append(t1 - t0)
+        e2e_s = reduce_max(statistics.mean(et), world)
+        line["e2e"] = {"value": whole_job_tflops(w.flop, world, e2e_s), "unit": UNIT,
+                       "h2d_bytes_per_step": x_np.nbytes + l_np.nbytes,
+                       "d2h_bytes_per_step": yh.numel() * 2 + sh.numel() * 4 + oh.numel() * 4 + gh.numel() * 4,
+                       "ms_per_step": e2e_s * 1e3, "api": "mk_moe_dispatch_gemm_host (pinned host buffers)"}
+        if rank == 0 and world == 1:
+            line["cpu_baseline"] = {k: v for k, v in oracle_sample(w, args.cpu_seconds, (x_np, l_np)).items()
+                                    if k != "seconds_estimated_full"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    w = synth.WORKLOADS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -87,7 +87,9 @@ typedef struct mk_config {
     int32_t debug_fault;    /* MK_FAULT_*                                        */
     int64_t spin_limit_ns;  /* bound on every device wait; 0 = 2 s               */
     int32_t trace;          /* 1 = record per-CTA %globaltimer phase stamps      */
-    int32_t reserved[7];    /* must be zero                                     */
+    int32_t l2_prefetch;    /* W K-blocks prefetched into L2 ahead of use;
+                               <= 0 = off (the default)                          */
+    int32_t reserved[6];    /* must be zero                                     */
 } mk_config_t;
 
 /* Per-launch facts, for tests and the benchmark. */

@@ -69,7 +69,8 @@ class mk_config_t(ctypes.Structure):
         ("debug_fault", ctypes.c_int32),
         ("spin_limit_ns", ctypes.c_int64),
         ("trace", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("l2_prefetch", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
 
@@ -230,10 +231,11 @@ def mk_release_workspace() -> None:
 # ------------------------------------------------------------- convenience --
 
 def make_config(mode=MK_MODE_FUSED, out_dtype=MK_OUT_BF16, dispatch_ctas=0, grid_ctas=0, n_group=0,
-                debug_fault=MK_FAULT_NONE, spin_limit_ns=0, trace=0) -> mk_config_t:
+                debug_fault=MK_FAULT_NONE, spin_limit_ns=0, trace=0, l2_prefetch=0) -> mk_config_t:
     c = mk_config_default()
     c.mode, c.out_dtype, c.dispatch_ctas, c.grid_ctas = mode, out_dtype, dispatch_ctas, grid_ctas
     c.n_group, c.debug_fault, c.spin_limit_ns, c.trace = n_group, debug_fault, spin_limit_ns, trace
+    c.l2_prefetch = l2_prefetch
     return c
 
 

@@ -225,7 +225,7 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
     mk_status_t s = validate_sizes(T, H, E, k, F);
     if (s != MK_OK) return s;
     const mk_config_t c = config_or_default(cfg_in);
-    for (int i = 0; i < 7; ++i)
+    for (int i = 0; i < 6; ++i)
         if (c.reserved[i] != 0) return MK_ERR_INVALID_ARG;
     if (c.mode < MK_MODE_FUSED || c.mode > MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
     if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
@@ -296,6 +296,9 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
         p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
     }
     p.debug_drop_tile = c.debug_fault == MK_FAULT_DROP_TILE_FLAG ? 0 : -1;
+    // measured on GB300: issuing L2 prefetches from the producer thread slows
+    // the loads behind them, so it is off unless asked for
+    p.l2_prefetch = c.l2_prefetch > 0 ? c.l2_prefetch : 0;
     p.trace = c.trace ? 1 : 0;
     p.spin_limit_ns = c.spin_limit_ns > 0 ? c.spin_limit_ns : kDefaultSpinNs;
     p.ctl = reinterpret_cast<Ctl*>(ws + L.ctl);

@@ -106,6 +106,7 @@ struct Params {
     int mode;
     int compute;             // 0: dispatch only
     int debug_drop_tile;     // tile whose flag is withheld (-1: none)
+    int l2_prefetch;         // W k-blocks prefetched into L2 ahead of the TMA loads (0: off)
     int trace;
     long long spin_limit_ns;
     // workspace

@@ -197,18 +197,25 @@ __device__ void route_chunk(const Params& p, int c) {
     }
     for (int e0 = 0; e0 < E; e0 += 64) {
         const int ne = min(64, E - e0);
-        __syncwarp();
-#pragma unroll 8
+        // All 32 rows' loads are issued before the first store to shared
+        // memory (explicit registers), so their latencies overlap.
+        float r0[32], r1[32];
+#pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int ti = tbase + i;
-            if (ti < T) {
-                const float* row = p.logits + size_t(ti) * E + e0;
-                if (lane < ne) slog[i * RT_LOGIT_STRIDE + lane] = __ldg(row + lane);
-                if (lane + 32 < ne) slog[i * RT_LOGIT_STRIDE + lane + 32] = __ldg(row + lane + 32);
-            }
+            const float* row = p.logits + size_t(ti < T ? ti : 0) * E + e0;
+            r0[i] = (ti < T && lane < ne) ? __ldg(row + lane) : 0.f;
+            r1[i] = (ti < T && lane + 32 < ne) ? __ldg(row + lane + 32) : 0.f;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            slog[i * RT_LOGIT_STRIDE + lane] = r0[i];
+            slog[i * RT_LOGIT_STRIDE + lane + 32] = r1[i];
         }
         __syncwarp();
         if (t < T) {
+#pragma unroll 4
             for (int ee = 0; ee < ne; ++ee) {
                 const float v = slog[lane * RT_LOGIT_STRIDE + ee];
                 const int e = e0 + ee;
@@ -352,7 +359,27 @@ __device__ void build_tables(const Params& p, CtrlSmem* cs) {
 // prefix (rows of earlier chunks) is kept in smem as the chunk's bases.
 __device__ void scan_counts(const Params& p, CtrlSmem* cs, bool keep_bases) {
     int* sbase = reinterpret_cast<int*>(smem_base() + RT_BASES);
+    int* scnt = reinterpret_cast<int*>(smem_base());  // routing scratch is dead by now
     const int E = p.E, nch = p.nch, grid = gridDim.x;
+    const int total = nch * E;
+    const bool in_smem = total <= RT_BASES / 4;
+    if (in_smem) {
+        // copy the counts table to shared memory, 8 independent loads per thread in flight
+        for (int b0 = 0; b0 < total; b0 += NTHREADS * 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = b0 + j * NTHREADS + threadIdx.x;
+                v[j] = i < total ? __ldcg(p.counts + i) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = b0 + j * NTHREADS + threadIdx.x;
+                if (i < total) scnt[i] = v[j];
+            }
+        }
+        __syncthreads();
+    }
     for (int e = threadIdx.x; e < E; e += NTHREADS) {
         int run = 0, m = 0;
         int mine = blockIdx.x;
@@ -362,7 +389,7 @@ __device__ void scan_counts(const Params& p, CtrlSmem* cs, bool keep_bases) {
                 ++m;
                 mine += grid;
             }
-            run += __ldcg(p.counts + size_t(c) * E + e);
+            run += in_smem ? scnt[c * E + e] : __ldcg(p.counts + size_t(c) * E + e);
         }
         cs->tot[e] = run;
     }
@@ -382,17 +409,32 @@ __device__ void scatter_chunk(const Params& p, int c, const int* cbase, const Wa
     const int k = p.k, T = p.T;
     const int t0 = c * ROUTE_CHUNK;
     const int n = min(ROUTE_CHUNK, T - t0) * k;
-    for (int i = threadIdx.x; i < n; i += NTHREADS) {
-        const int q = t0 * k + i;
-        const int e = __ldcg(p.topk_idx + q);
-        const int dest = cbase[e] + __ldcg(p.lrank + q);
-        if (dest < 0 || dest >= p.rows) {
-            record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(dest));
-            raise_abort(w);
-            continue;
+    constexpr int U = 4;  // entries per thread per batch: loads issued before the stores
+    for (int i0 = threadIdx.x; i0 < n; i0 += NTHREADS * U) {
+        int e[U], lr[U];
+        float g[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * NTHREADS;
+            const int q = t0 * k + (i < n ? i : 0);
+            e[u] = __ldcg(p.topk_idx + q);
+            lr[u] = __ldcg(p.lrank + q);
+            g[u] = __ldcg(p.topk_gate + q);
         }
-        p.src_index[dest] = q;
-        p.gate_w[dest] = __ldcg(p.topk_gate + q);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * NTHREADS;
+            if (i >= n) continue;
+            const int q = t0 * k + i;
+            const int dest = cbase[min(max(e[u], 0), MAX_E - 1)] + lr[u];
+            if (dest < 0 || dest >= p.rows) {
+                record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(dest));
+                raise_abort(w);
+                continue;
+            }
+            p.src_index[dest] = q;
+            p.gate_w[dest] = g[u];
+        }
     }
 }
 
@@ -544,6 +586,10 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* s = smem_base();
     const int total_items = cs->item_start[p.E];
+    // Waits inside the pipeline only stall because something upstream (a
+    // tile flag, a barrier) stalls: they get twice the limit, so the wait
+    // that times out and is recorded is the one at the root.
+    const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
 
     if (warp == 0) {
         if (lane == 0) {
@@ -555,7 +601,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             for (uint32_t it = 0; ok; ++it) {
                 const int item = int(next);
                 const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
-                if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, w, SITE_INFO_EMPTY)) {
+                if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
                     ok = false;
                     break;
                 }
@@ -568,6 +614,17 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 Info inf;
                 int gtile;
                 decode_item(p, cs, item, inf, gtile);
+                const int pf = p.l2_prefetch;
+                if (pf > 0) {
+                    // the first k-blocks of this item's weight slice head for L2 now
+                    const int n0 = min(pf, p.kblocks);
+                    for (int kb = 0; kb < n0; ++kb)
+#pragma unroll
+                        for (int q = 0; q < BN / 64; ++q) {
+                            const int col = inf.nbk * BN + q * 64;
+                            if (col < p.F) tma_prefetch_l2_2d(tmB, col, inf.e * p.H + kb * BK);
+                        }
+                }
                 cs->info[slot] = inf;
                 mbar_arrive(&cs->info_full[slot]);
                 if (wait_ready) {
@@ -579,9 +636,16 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 }
                 const int ncol = p.F;
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!wait_mbar(&cs->empty[stage], phase ^ 1u, w, SITE_STAGE_EMPTY)) {
+                    if (!wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
                         ok = false;
                         break;
+                    }
+                    if (pf > 0 && kb + pf < p.kblocks) {
+#pragma unroll
+                        for (int q = 0; q < BN / 64; ++q) {
+                            const int col = inf.nbk * BN + q * 64;
+                            if (col < ncol) tma_prefetch_l2_2d(tmB, col, inf.e * p.H + (kb + pf) * BK);
+                        }
                     }
                     uint64_t* fb = &cs->full[stage];
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
@@ -617,16 +681,16 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             bool issued = false;
             for (uint32_t it = 0;; ++it) {
                 const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
-                if (!wait_mbar(&cs->info_full[slot], iph, w, SITE_INFO_FULL)) break;
+                if (!wait_mbar(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
                 const int e = cs->info[slot].e;
                 mbar_arrive(&cs->info_empty[slot]);
                 if (e < 0) break;
-                if (!wait_mbar(&cs->acc_empty[acc], accph ^ 1u, w, SITE_ACC_EMPTY)) break;
+                if (!wait_mbar(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
                 tc_fence_after();
                 const uint32_t d = cs->tmem_base + acc * BN;
                 bool ok = true;
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!wait_mbar(&cs->full[stage], phase, w, SITE_STAGE_FULL)) {
+                    if (!wait_mbar(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
                         ok = false;
                         break;
                     }
@@ -668,12 +732,12 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
         uint32_t acc = 0, accph = 0;
         for (uint32_t it = 0;; ++it) {
             const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
-            if (!wait_mbar(&cs->info_full[slot], iph, w, SITE_INFO_FULL)) break;
+            if (!wait_mbar(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
             const Info inf = cs->info[slot];
             __syncwarp();
             if (lane == 0) mbar_arrive(&cs->info_empty[slot]);
             if (inf.e < 0) break;
-            if (!wait_mbar(&cs->acc_full[acc], accph, w, SITE_ACC_FULL)) break;
+            if (!wait_mbar(&cs->acc_full[acc], accph, wp, SITE_ACC_FULL)) break;
             tc_fence_after();
             const int rloc = quad * 32 + lane;
             const bool rowok = rloc < inf.nrows;

@@ -49,7 +49,7 @@ def test_status_strings(lib):
 def test_config_defaults(lib):
     c = mk.mk_config_default()
     assert c.mode == mk.MK_MODE_FUSED and c.out_dtype == mk.MK_OUT_BF16
-    assert c.dispatch_ctas == 0 and c.spin_limit_ns == 0 and list(c.reserved) == [0] * 7
+    assert c.dispatch_ctas == 0 and c.spin_limit_ns == 0 and list(c.reserved) == [0] * 6 and c.l2_prefetch == 0
 
 
 @pytest.mark.parametrize("T,H,E,k,F,want", [

@@ -131,6 +131,32 @@ mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_ho
                                       int32_t* src_index_host, int32_t* expert_offsets_host,
                                       float* gate_w_host, void* stream, const mk_config_t* cfg);
 
+/* Size of the fixed device array that mk_moe_dispatch_gemm_noalloc works in. */
+#define MK_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* Allocation-free variant of mk_moe_dispatch_gemm_ex (the pages have no
+ * counterpart: it serves callers of this library that may not allocate
+ * device memory while they run it -- a host framework that owns the whole
+ * device-memory budget through its own allocator, or a latency-critical
+ * decode loop where cudaMalloc and its possible device-wide synchronisation
+ * are not allowed).  Same arguments and outputs as the allocating path; the
+ * caller still passes every input and output.  Instead of a workspace it
+ * uses one static device array of MK_NOALLOC_SCRATCH_BYTES (64 MiB), which
+ * each GPU where it is set up keeps until the process exits.  Calls whose
+ * mk_workspace_size() exceeds that return MK_ERR_WORKSPACE and launch
+ * nothing (it fits decode-sized batches: about T*k*H*2 bytes of staged rows
+ * plus small tables).  No cudaMalloc, cudaFree or allocating library call
+ * is made.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the array and
+ * finds the previous call's contents there (the call clears what must start
+ * at zero), so calls that overlap on the GPU -- on different streams, or
+ * from different threads -- race: serialise them. */
+mk_status_t mk_moe_dispatch_gemm_noalloc(const void* x, const float* logits, int T, int H, int E, int k,
+                                         const void* W, int F, void* y_sorted, int32_t* src_index,
+                                         int32_t* expert_offsets, float* gate_w, void* stream,
+                                         const mk_config_t* cfg);
+
 /* Bytes of workspace a call with these sizes needs (0 on invalid sizes). */
 size_t mk_workspace_size(int T, int H, int F, int E, int k, const mk_config_t* cfg);
 

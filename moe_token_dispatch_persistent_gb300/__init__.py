@@ -38,6 +38,7 @@ ABI_FUNCTIONS = (
     "mk_moe_dispatch_gemm",
     "mk_moe_dispatch_gemm_ex",
     "mk_moe_dispatch_gemm_host",
+    "mk_moe_dispatch_gemm_noalloc",
     "mk_workspace_size",
     "mk_get_status",
     "mk_last_error_detail",
@@ -107,6 +108,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     h.mk_moe_dispatch_gemm_ex.restype = _i
     h.mk_moe_dispatch_gemm_host.argtypes = sig + [ctypes.POINTER(mk_config_t)]
     h.mk_moe_dispatch_gemm_host.restype = _i
+    h.mk_moe_dispatch_gemm_noalloc.argtypes = sig + [ctypes.POINTER(mk_config_t)]
+    h.mk_moe_dispatch_gemm_noalloc.restype = _i
     h.mk_workspace_size.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(mk_config_t)]
     h.mk_workspace_size.restype = ctypes.c_size_t
     h.mk_get_status.argtypes = [_p]
@@ -198,6 +201,20 @@ def mk_moe_dispatch_gemm_host(x_host, logits_host, T, H, E, k, W, F, y_host, src
     return int(lib().mk_moe_dispatch_gemm_host(_ptr(x_host), _ptr(logits_host), T, H, E, k, _ptr(W), F,
                                                _ptr(y_host), _ptr(src_host), _ptr(offsets_host), _ptr(gate_host),
                                                _stream(stream), ctypes.byref(cfg) if cfg is not None else None))
+
+
+MK_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def mk_moe_dispatch_gemm_noalloc(x, logits, T, H, E, k, W, F, y_sorted, src_index, expert_offsets, gate_w,
+                                 stream=None, cfg: mk_config_t | None = None) -> int:
+    """Allocation-free call: the library's fixed 64 MiB device array is the
+    workspace (for callers that may not allocate device memory while they
+    run this, e.g. inside a framework that owns the device-memory budget).
+    Calls that overlap on the GPU share that array and race."""
+    return int(lib().mk_moe_dispatch_gemm_noalloc(_ptr(x), _ptr(logits), T, H, E, k, _ptr(W), F, _ptr(y_sorted),
+                                                  _ptr(src_index), _ptr(expert_offsets), _ptr(gate_w),
+                                                  _stream(stream), ctypes.byref(cfg) if cfg is not None else None))
 
 
 def mk_get_status(stream=None) -> int:

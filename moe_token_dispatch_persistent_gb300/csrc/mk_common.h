@@ -58,7 +58,7 @@ struct Ctl {
     uint32_t next_tile;      // gather queue (dispatch role)
     uint32_t next_item;      // GEMM work queue (compute role)
     uint32_t abort;          // 1 once any CTA of this call gave up
-    uint32_t items_done;
+    uint32_t tiles_done;     // tiles the dispatch role has gathered and flagged
     uint32_t pad[56];
 };
 static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");

@@ -505,6 +505,9 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, uint32_t flag, const 
         if (lane == 0 && ok && tile != p.debug_drop_tile) {
             __threadfence();
             st_release_u32(p.ready + tile, flag);
+            // count of tiles gathered so far: once it reaches the tile count a
+            // single acquire of it stands in for every per-tile flag
+            atom_add_acq_rel_u32(&p.ctl->tiles_done, 1u);
         }
         if (aborted(w)) break;
     }
@@ -598,6 +601,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             uint32_t issued_par = 0, issued_any = 0;  // per-stage bit: parity of the last issue
             bool ok = true;
             uint32_t next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+            const int ntiles = cs->tile_start[p.E];
             for (uint32_t it = 0; ok; ++it) {
                 const int item = int(next);
                 const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
@@ -628,7 +632,10 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 cs->info[slot] = inf;
                 mbar_arrive(&cs->info_full[slot]);
                 if (wait_ready) {
-                    if (!wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
+                    // one acquire per item until every tile is known to be in
+                    if (ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles)) {
+                        wait_ready = false;
+                    } else if (!wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
                         ok = false;
                         break;
                     }
@@ -828,7 +835,7 @@ __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
             c->bar_scattered = 0;
             c->next_tile = 0;
             c->next_item = 0;
-            c->items_done = 0;
+            c->tiles_done = 0;
             c->abort = 0;
             c->epoch = c->epoch + 1u;  // calls completed on this workspace
             c->exit_count = 0;

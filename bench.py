@@ -67,6 +67,29 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def ncu_traffic(workload_name: str):
+    """DRAM bytes (read + write) per launch of the fused kernel from the
+    committed ncu capture of this workload, or None when there is none or the
+    kernel sources changed since it was taken."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f).get(workload_name)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    try:
+        for src in rec["kernel_sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if h.hexdigest() == rec["kernel_sha256"] else None
+
+
 def workload_config(w: synth.Workload, extra=None):
     c = {"workload": w.describe(), "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k, "seed": w.seed,
          "l2": "flushed between timed steps (256 MiB write, outside the events)"}
@@ -341,7 +364,7 @@ def run_ours(args, w):
                                       "active_experts": active}),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"bf16_tflops (burst), {peaks_src}",
-                     "kernel": "mk_fused_kernel", "traffic": None,
+                     "kernel": "mk_fused_kernel", "traffic": ncu_traffic(w.name),
                      "compulsory_bytes": compulsory_bytes(w, active)},
         "gpu_launches": gpu_launches,
         "clocks": clocks,

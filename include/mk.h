@@ -89,8 +89,16 @@ typedef struct mk_config {
     int32_t trace;          /* 1 = record per-CTA %globaltimer phase stamps      */
     int32_t l2_prefetch;    /* W K-blocks prefetched into L2 ahead of use;
                                <= 0 = off (the default)                          */
-    int32_t reserved[6];    /* must be zero                                     */
+    int32_t mma_pair;       /* MK_MMA_*: one SM per 128-row tile, or an SM pair
+                               (cta_group::2) per 256-row tile                  */
+    int32_t reserved[5];    /* must be zero                                     */
 } mk_config_t;
+
+/* Expert GEMM tile.  SINGLE: each CTA runs a 128 x 256 tile alone.  PAIR: a
+ * cluster of two CTAs (two SMs) runs a 256 x 256 tile with the 2-SM tensor
+ * core instruction; each SM stages half the operands, so the same shared
+ * memory holds six stages instead of four.  AUTO picks per shape. */
+enum { MK_MMA_AUTO = 0, MK_MMA_SINGLE = 1, MK_MMA_PAIR = 2 };
 
 /* Per-launch facts, for tests and the benchmark. */
 typedef struct mk_launch_info {
@@ -99,6 +107,8 @@ typedef struct mk_launch_info {
     int32_t launches;       /* kernels launched by the last call      */
     int32_t n_group;
     int64_t workspace_bytes;
+    int32_t mma_pair;       /* MK_MMA_SINGLE or MK_MMA_PAIR as resolved */
+    int32_t reserved0;
 } mk_launch_info_t;
 
 /* Fill `cfg` with the defaults (fused, bf16 output, heuristic split). */

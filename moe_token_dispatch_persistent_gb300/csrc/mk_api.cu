@@ -140,6 +140,15 @@ int dispatch_split(int grid, int T, int H, int F, int k) {
     return d;
 }
 
+// Tile height: SM pairs (256-row tiles, 2-SM MMA) unless asked otherwise.
+// AUTO keeps single-SM tiles until the pair path is measured on a shape.
+int resolve_pair(const mk_config_t& c, int T, int E, int k) {
+    (void)T;
+    (void)E;
+    (void)k;
+    return c.mma_pair == MK_MMA_PAIR ? MK_MMA_PAIR : MK_MMA_SINGLE;
+}
+
 // Work order within an expert: whole expert weight reused through L2 when it
 // is small (N-group = all N-blocks, tiles outer); otherwise groups of
 // N-blocks whose weight slice is ~16 MB.
@@ -225,8 +234,9 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
     mk_status_t s = validate_sizes(T, H, E, k, F);
     if (s != MK_OK) return s;
     const mk_config_t c = config_or_default(cfg_in);
-    for (int i = 0; i < 6; ++i)
+    for (int i = 0; i < 5; ++i)
         if (c.reserved[i] != 0) return MK_ERR_INVALID_ARG;
+    if (c.mma_pair < MK_MMA_AUTO || c.mma_pair > MK_MMA_PAIR) return MK_ERR_INVALID_ARG;
     if (c.mode < MK_MODE_FUSED || c.mode > MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
     if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
     if (c.debug_fault != MK_FAULT_NONE && c.debug_fault != MK_FAULT_DROP_TILE_FLAG) return MK_ERR_INVALID_ARG;
@@ -250,7 +260,10 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
         return cudaMemsetAsync(expert_offsets, 0, size_t(E + 1) * 4, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
     }
 
-    const int grid = grid_for(*d, c);
+    const bool pair = resolve_pair(c, T, E, k) == MK_MMA_PAIR;
+    int grid = grid_for(*d, c);
+    if (pair) grid &= ~1;  // whole clusters of two
+    if (grid < (pair ? 2 : 1)) return MK_ERR_UNSUPPORTED;
     const int rows = T * k;
     const int nch = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
     if (nch > grid * MAX_CHUNKS_PER_CTA) return MK_ERR_UNSUPPORTED;
@@ -290,7 +303,11 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
     } else {
         p.dispatch_ctas = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
         if (p.dispatch_ctas > grid) p.dispatch_ctas = grid;
+        if (pair) p.dispatch_ctas = (p.dispatch_ctas + 1) & ~1;  // both CTAs of a cluster share a role
+        if (p.dispatch_ctas > grid) p.dispatch_ctas = grid;
     }
+    p.pair = pair ? 1 : 0;
+    p.tile_rows = pair ? PAIR_TILE_M : BM;
     {
         int slots = int((SM_STAGE_END) / (size_t(H) * 2));
         p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
@@ -310,7 +327,7 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
     p.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
     p.xs = reinterpret_cast<uint16_t*>(ws + L.xs);
     p.trace_buf = reinterpret_cast<unsigned long long*>(ws + L.trace);
-    p.max_tiles = (rows + BM - 1) / BM + E;
+    p.max_tiles = (rows + p.tile_rows - 1) / p.tile_rows + E;
 
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof(tmA));
@@ -334,6 +351,7 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
     g_last_info.grid_ctas = grid;
     g_last_info.dispatch_ctas = c.mode == MK_MODE_UNFUSED ? 0 : p.dispatch_ctas;
     g_last_info.n_group = p.n_group;
+    g_last_info.mma_pair = pair ? MK_MMA_PAIR : MK_MMA_SINGLE;
     g_last_info.workspace_bytes = int64_t(L.total);
     if (getenv("MK_LOG"))
         fprintf(stderr, "[mk] T=%d H=%d F=%d E=%d k=%d mode=%d grid=%d dispatch=%d n_group=%d slots=%d ws=%zu\n", T, H,

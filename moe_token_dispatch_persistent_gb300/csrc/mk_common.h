@@ -28,6 +28,17 @@ constexpr int MAX_CHUNKS_PER_CTA = 16;
 constexpr int MAX_GATHER_SLOTS = 32;
 constexpr int TRACE_SLOTS = 16;
 
+// CTA-pair variant (cta_group::2): a 256 x 256 tile per pair of SMs; each
+// CTA stages its 128 rows of A and 128 of B's 256 columns, so a stage is
+// 32 KiB and six fit where four single-CTA stages did.
+constexpr int PAIR_TILE_M = 2 * BM;
+constexpr int PSTAGES = 6;
+constexpr int PA_STAGE_BYTES = BM * BK * 2;                // 16 KiB (own 128 rows)
+constexpr int PB_STAGE_BYTES = BK * (BN / 2) * 2;          // 16 KiB (own 128 columns)
+constexpr int SM_PA = 0;
+constexpr int SM_PB = SM_PA + PSTAGES * PA_STAGE_BYTES;    // 96 KiB
+constexpr int MAX_STAGES = PSTAGES > STAGES ? PSTAGES : STAGES;
+
 // Dynamic shared memory map (offsets from a 1024-byte aligned base).
 constexpr int SM_A = 0;
 constexpr int SM_B = SM_A + STAGES * A_STAGE_BYTES;           // 64 KiB
@@ -46,6 +57,7 @@ constexpr int RT_WCNT = RT_LRANK + NWARPS * 32 * MAX_K * 4;
 constexpr int RT_BASES = RT_WCNT + NWARPS * MAX_E * 4;
 constexpr int RT_END = RT_BASES + MAX_CHUNKS_PER_CTA * MAX_E * 4;
 static_assert(RT_END <= SM_STAGE_END, "routing scratch must fit in the stage area");
+static_assert(SM_PB + PSTAGES * PB_STAGE_BYTES <= SM_STAGE_END, "pair stages must fit in the stage area");
 
 // Control block at the head of the workspace.  The kernels leave it ready
 // for the next call: the last CTA to exit zeroes the counters and the abort
@@ -107,6 +119,8 @@ struct Params {
     int compute;             // 0: dispatch only
     int debug_drop_tile;     // tile whose flag is withheld (-1: none)
     int l2_prefetch;         // W k-blocks prefetched into L2 ahead of the TMA loads (0: off)
+    int pair;                // 1: 2-SM MMA (cluster of 2 CTAs per 256-row tile)
+    int tile_rows;           // rows per tile: 128, or 256 with pair
     int trace;
     long long spin_limit_ns;
     // workspace

@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstddef>
 
 #include "mk_common.h"
 #include "mk_ptx.cuh"
@@ -137,13 +138,13 @@ __device__ __forceinline__ void stamp(const Params& p, int slot) {
 
 // ------------------------------------------------------ shared control -----
 
-struct Info {
+struct alignas(16) Info {  // 16-byte aligned: sent to the peer CTA with one v4 store
     int e, row0, nrows, nbk;
 };
 
 struct CtrlSmem {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t info_full[4];
@@ -159,6 +160,7 @@ struct CtrlSmem {
     int32_t tot[MAX_E];
 };
 static_assert(sizeof(CtrlSmem) <= SM_CTRL_BYTES, "control smem too large");
+static_assert(offsetof(CtrlSmem, info) % 16 == 0, "info slots must allow 16-byte stores");
 
 __device__ __forceinline__ uint8_t* smem_base() {
     extern __shared__ uint8_t smem_raw[];
@@ -318,7 +320,7 @@ __device__ void build_tables(const Params& p, CtrlSmem* cs) {
     for (int i = 0; i < 8; ++i) {
         const int e = lane * 8 + i;
         const int v = (e < E) ? cs->tot[e] : 0;
-        const int nt = (v + BM - 1) / BM;
+        const int nt = (v + p.tile_rows - 1) / p.tile_rows;
         lo[i] = so;
         lt[i] = st;
         li[i] = si;
@@ -470,8 +472,8 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, uint32_t flag, const 
         tile = __shfl_sync(0xffffffffu, tile, 0);
         if (tile >= ntiles) break;
         const int e = find_expert(cs->tile_start, p.E, tile);
-        const int row0 = cs->offs[e] + (tile - cs->tile_start[e]) * BM;
-        const int nrows = min(BM, cs->offs[e + 1] - row0);
+        const int row0 = cs->offs[e] + (tile - cs->tile_start[e]) * p.tile_rows;
+        const int nrows = min(p.tile_rows, cs->offs[e + 1] - row0);
         if (lane < nslot) {
             uint8_t* slot = s + size_t(lane) * row_bytes;
             for (int i = lane; i < nrows && ok; i += nslot) {
@@ -574,8 +576,8 @@ __device__ __forceinline__ void decode_item(const Params& p, const CtrlSmem* cs,
         nbk = full * G + (l2 - t_in * Gl);
     }
     inf.e = e;
-    inf.row0 = cs->offs[e] + t_in * BM;
-    inf.nrows = min(BM, cs->offs[e + 1] - inf.row0);
+    inf.row0 = cs->offs[e] + t_in * p.tile_rows;
+    inf.nrows = min(p.tile_rows, cs->offs[e + 1] - inf.row0);
     inf.nbk = nbk;
     gtile = cs->tile_start[e] + t_in;
 }
@@ -790,41 +792,281 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
 
 // ----------------------------------------------------------- CTA setup -----
 
+// Bounded wait with cluster-scope acquire (arrivals may come from the peer CTA
+// or from the pair's tensor core).
+__device__ __forceinline__ bool wait_mbar_cl(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t n = 0;
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if ((++n & 63u) == 0u) {
+            if (aborted(w)) return false;
+            if ((long long)(globaltimer() - t0) > w.limit_ns) {
+                record_error(ERR_TIMEOUT, site, parity);
+                raise_abort(w);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+constexpr uint32_t IDESC_PAIR = umma_idesc_bf16(PAIR_TILE_M, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+
+// CTA-pair compute role (cluster of two CTAs, cta_group::2): one 256 x 256
+// tile per pair.  Rank 0 (the leader) takes work items from the queue and
+// writes each item's description into both CTAs' shared memory; both CTAs'
+// producers load their own 128 rows of A and their own 128 of B's columns
+// into their 6-stage rings, the bytes of both counted on the leader's full
+// barrier; one leader thread issues the 2-SM MMAs, whose commits release the
+// stage and hand over the accumulator in both CTAs at once (multicast); each
+// CTA's epilogue drains its own 128 TMEM lanes (rows rank*128 + ...) and
+// tells the leader (remote arrive) when the accumulator is free again.
+__device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, CtrlSmem* cs,
+                                  bool wait_ready, uint32_t flag, const WaitCtx& w) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    uint8_t* s = smem_base();
+    const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
+    const int total_items = cs->item_start[p.E];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer (both CTAs) ----------------
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_par = 0, issued_any = 0;
+            bool ok = true;
+            uint32_t next = leader ? atom_add_relaxed_u32(&p.ctl->next_item, 1u) : 0u;
+            const int ntiles = cs->tile_start[p.E];
+            const uint32_t full_leader = mapa_shared(smem_u32(&cs->full[0]), 0);
+            for (uint32_t it = 0; ok; ++it) {
+                const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+                Info inf{-1, 0, 0, 0};
+                int gtile = 0;
+                if (leader) {
+                    const int item = int(next);
+                    if (!wait_mbar_cl(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    if (item < total_items) {
+                        next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+                        decode_item(p, cs, item, inf, gtile);
+                    }
+                    cs->info[slot] = inf;
+                    st_cluster_v4(mapa_shared(smem_u32(&cs->info[slot]), 1), inf.e, inf.row0, inf.nrows, inf.nbk);
+                    mbar_arrive(&cs->info_full[slot]);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&cs->info_full[slot]), 1));
+                } else {
+                    if (!wait_mbar_cl(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    inf = cs->info[slot];
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&cs->info_empty[slot]), 0));
+                    if (inf.e >= 0) gtile = cs->tile_start[inf.e] + (inf.row0 - cs->offs[inf.e]) / p.tile_rows;
+                }
+                if (inf.e < 0) break;
+                if (wait_ready) {
+                    if (ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles)) {
+                        wait_ready = false;
+                    } else if (!wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async();
+                }
+                const int arow = inf.row0 + int(rank) * BM;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!wait_mbar_cl(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(&cs->full[stage], 2 * (PA_STAGE_BYTES + PB_STAGE_BYTES));
+                    const uint32_t fb = full_leader + stage * uint32_t(sizeof(uint64_t));
+                    tma_load_2d_pair(s + SM_PA + stage * PA_STAGE_BYTES, tmA, kb * BK, arow, fb);
+                    uint8_t* b = s + SM_PB + stage * PB_STAGE_BYTES;
+#pragma unroll
+                    for (int q = 0; q < BN / 128; ++q) {
+                        const int col = inf.nbk * BN + int(rank) * (BN / 2) + q * 64;
+                        tma_load_2d_pair(b + q * B_CHUNK_BYTES, tmB, col < p.F ? col : p.F, inf.e * p.H + kb * BK,
+                                         fb);
+                    }
+                    issued_any |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && leader) {
+                WaitCtx shortw{nullptr, 0u, 5000000LL};
+                for (int st = 0; st < PSTAGES; ++st)
+                    if (issued_any & (1u << st))
+                        wait_mbar_cl(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            // ---------------- 2-SM MMA issuer (leader only) ----------------
+            uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
+            bool issued = false;
+            for (uint32_t it = 0;; ++it) {
+                const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+                if (!wait_mbar_cl(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
+                const int e = cs->info[slot].e;
+                mbar_arrive(&cs->info_empty[slot]);
+                if (e < 0) break;
+                if (!wait_mbar_cl(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
+                tc_fence_after();
+                const uint32_t d = cs->tmem_base + acc * BN;
+                bool ok = true;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!wait_mbar_cl(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(s + SM_PA + stage * PA_STAGE_BYTES);
+                    const uint32_t b0 = smem_u32(s + SM_PB + stage * PB_STAGE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // the peer's rows / columns sit at the same offsets in its shared memory
+                        const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
+                        tc_mma_f16_pair(d, ad, bd, IDESC_PAIR, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit_pair_multicast(&cs->empty[stage], 0x3);
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(&cs->acc_full[acc], 0x3);
+                acc ^= 1u;
+                if (acc == 0) accph ^= 1u;
+            }
+            if (issued) {
+                tc_commit_pair(&cs->drain);
+                WaitCtx shortw{nullptr, 0u, 5000000LL};
+                wait_mbar_cl(&cs->drain, 0u, shortw, SITE_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warps 2..5 of both CTAs ----------------
+        const int quad = warp & 3;
+        const uint32_t info_empty_leader = mapa_shared(smem_u32(&cs->info_empty[0]), 0);
+        const uint32_t acc_empty_leader = mapa_shared(smem_u32(&cs->acc_empty[0]), 0);
+        uint32_t acc = 0, accph = 0;
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+            if (!wait_mbar_cl(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
+            const Info inf = cs->info[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(info_empty_leader + slot * uint32_t(sizeof(uint64_t)));
+            if (inf.e < 0) break;
+            if (!wait_mbar_cl(&cs->acc_full[acc], accph, wp, SITE_ACC_FULL)) break;
+            tc_fence_after();
+            const int rloc = int(rank) * BM + quad * 32 + lane;
+            const bool rowok = rloc < inf.nrows;
+            const size_t row = size_t(inf.row0) + rloc;
+            const int n0 = inf.nbk * BN;
+            const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                const int col = n0 + cc * 32;
+                if (col >= p.F) break;
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                tmem_ld_wait();
+                if (rowok) {
+                    if (p.out_f32) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.y) + row * p.F + col);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + row * p.F + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * u]),
+                                                                               __uint_as_float(r[8 * v + 2 * u + 1]));
+                                pk[u] = *reinterpret_cast<const uint32_t*>(&h);
+                            }
+                            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader + acc * uint32_t(sizeof(uint64_t)));
+            acc ^= 1u;
+            if (acc == 0) accph ^= 1u;
+        }
+    }
+}
+
+// Barrier arrival counts.  Single CTA: the producer's expect-tx, one commit,
+// 128 epilogue threads, the MMA thread + 4 epilogue warps.  Pair: acc_empty
+// gets one arrival per epilogue warp of both CTAs (8) and info_empty the
+// leader's MMA thread and 4 epilogue warps plus the peer's producer and 4
+// epilogue warps (10); those two live in the leader only.
+template <int PAIR>
 __device__ void cta_setup(CtrlSmem* cs, bool with_tmem) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < MAX_STAGES; ++i) {
             mbar_init(&cs->full[i], 1);
             mbar_init(&cs->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&cs->acc_full[i], 1);
-            mbar_init(&cs->acc_empty[i], 128);
+            mbar_init(&cs->acc_empty[i], PAIR ? 8 : 128);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&cs->info_full[i], 1);
-            mbar_init(&cs->info_empty[i], 1 + 4);
+            mbar_init(&cs->info_empty[i], PAIR ? 10 : 1 + 4);
         }
         mbar_init(&cs->drain, 1);
         for (int i = 0; i < MAX_GATHER_SLOTS; ++i) mbar_init(&cs->gbar[i], 1);
         fence_barrier_init();
     }
+    if (PAIR) cluster_sync();  // peer running and its barriers initialised before any remote use
     if (with_tmem && warp == 1) {
-        tmem_alloc(&cs->tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(&cs->tmem_base, TMEM_COLS);  // collective with the peer's warp 1
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&cs->tmem_base, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 }
 
+template <int PAIR>
 __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs done with the pair's MMAs before the collective free
     if (with_tmem && (threadIdx.x >> 5) == 1) {
         tc_fence_after();
-        tmem_dealloc(cs->tmem_base, TMEM_COLS);
+        if (PAIR) tmem_dealloc_pair(cs->tmem_base, TMEM_COLS);
+        else tmem_dealloc(cs->tmem_base, TMEM_COLS);
     }
+    if (PAIR) cluster_sync();  // neither CTA leaves while the other may touch its shared memory
     if (threadIdx.x == 0) {
         if (p.trace) p.trace_buf[blockIdx.x * TRACE_SLOTS + 15] = globaltimer();
         const uint32_t old = atom_add_acq_rel_u32(&p.ctl->exit_count, 1u);
@@ -846,6 +1088,7 @@ __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
 
 // ------------------------------------------------------------- kernels -----
 
+template <int PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mk_fused_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
     CtrlSmem* cs = ctrl();
@@ -857,7 +1100,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    cta_setup(cs, p.compute != 0);
+    cta_setup<PAIR>(cs, p.compute != 0);
 
     // This call's readiness flags start at 0.  Cleared before the routing
     // barrier; they are set only after it, so no stale value is ever seen.
@@ -910,11 +1153,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncthreads();
         if (cs->bcast[2]) {
             stamp(p, 6);
-            compute_role(p, &tmA, &tmB, cs, true, flag, w);
+            if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, true, flag, w);
+            else compute_role(p, &tmA, &tmB, cs, true, flag, w);
             stamp(p, 7);
         }
     }
-    cta_teardown(p, cs, p.compute != 0);
+    cta_teardown<PAIR>(p, cs, p.compute != 0);
 }
 
 // Unfused baseline, launch 1: routing per chunk.
@@ -959,6 +1203,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_gather_kernel(const Params p) 
 }
 
 // Unfused baseline, launch 4: persistent expert GEMM over all tiles.
+template <int PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mk_gemm_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
     CtrlSmem* cs = ctrl();
@@ -968,29 +1213,51 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    cta_setup(cs, true);
+    cta_setup<PAIR>(cs, true);
     for (int e = threadIdx.x; e < p.E; e += NTHREADS) cs->tot[e] = p.expert_offsets[e + 1] - p.expert_offsets[e];
     __syncthreads();
     build_tables(p, cs);
     __syncthreads();
-    compute_role(p, &tmA, &tmB, cs, false, flag, w);
-    cta_teardown(p, cs, true);
+    if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, false, flag, w);
+    else compute_role(p, &tmA, &tmB, cs, false, flag, w);
+    cta_teardown<PAIR>(p, cs, true);
 }
 
 // ---------------------------------------------------------- host hooks -----
 
+// The persistent kernels wait on each other, so every CTA must be resident:
+// a cooperative launch guarantees it or fails.  The pair kernel also needs
+// clusters of two; if the driver refuses the cooperative attribute together
+// with clusters, it is launched without it after an occupancy check that
+// every cluster fits at once.
 cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (they wait on each other)
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
+    if (!p.pair) {
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, mk_fused_kernel<0>, p, a, b);
+    }
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b);
+    if (err == cudaSuccess) return err;
+    (void)cudaGetLastError();
+    cfg.attrs = attr + 1;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mk_fused_kernel, p, a, b);
+    int clusters = 0;
+    if ((err = cudaOccupancyMaxActiveClusters(&clusters, mk_fused_kernel<1>, &cfg)) != cudaSuccess) return err;
+    if (2 * clusters < grid) return cudaErrorCooperativeLaunchTooLarge;
+    return cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b);
 }
 
 cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st) {
@@ -1001,13 +1268,30 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     mk_gather_kernel<<<p.nch, NTHREADS, SMEM_BYTES, st>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    mk_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b);
-    return cudaGetLastError();
+    if (!p.pair) {
+        mk_gemm_kernel<0><<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b);
 }
 
 cudaError_t set_kernel_attributes() {
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(mk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+    if ((err = cudaFuncSetAttribute(mk_fused_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+        return err;
+    if ((err = cudaFuncSetAttribute(mk_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
         return err;
     if ((err = cudaFuncSetAttribute(mk_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
         return err;
@@ -1015,11 +1299,13 @@ cudaError_t set_kernel_attributes() {
         return err;
     if ((err = cudaFuncSetAttribute(mk_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
         return err;
-    return cudaFuncSetAttribute(mk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if ((err = cudaFuncSetAttribute(mk_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+        return err;
+    return cudaFuncSetAttribute(mk_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
 }
 
 cudaError_t fused_max_blocks_per_sm(int* n) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, mk_fused_kernel, NTHREADS, SMEM_BYTES);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, mk_fused_kernel<0>, NTHREADS, SMEM_BYTES);
 }
 
 cudaError_t read_and_clear_error(uint32_t out[4], cudaStream_t st) {

@@ -116,6 +116,23 @@ int mko_dispatch(const int32_t* topk_idx, const float* topk_gate,
     return MKO_OK;
 }
 
+int mko_combine(const double* y, const int32_t* src_index, const float* gate_w,
+                int64_t T, int k, int F, double* out) {
+    if (T < 0 || k < 1 || F < 1) return MKO_EARG;
+    if (T > 0 && (!y || !src_index || !gate_w || !out)) return MKO_EARG;
+    const int64_t n = T * (int64_t)k;
+    for (int64_t r = 0; r < n; ++r)
+        if (src_index[r] < 0 || src_index[r] >= n) return MKO_EARG;
+    for (int64_t i = 0; i < T * (int64_t)F; ++i) out[i] = 0.0;
+    /* every sorted row adds its gated product to its token's row */
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t t = src_index[r] / k;
+        const double g = (double)gate_w[r];
+        for (int f = 0; f < F; ++f) out[t * F + f] += g * y[r * F + f];
+    }
+    return MKO_OK;
+}
+
 int mko_expert_rows(const uint16_t* x, const uint16_t* W,
                     int64_t T, int H, int F, int E, int k,
                     const int32_t* expert_offsets, const int32_t* src_index,

@@ -63,6 +63,14 @@ int mko_expert_rows(const uint16_t* x, const uint16_t* W,
                     const int32_t* expert_offsets, const int32_t* src_index,
                     const int64_t* rows, int64_t n, double* y);
 
+/* Combine (the step after the expert product, which completes an MoE layer):
+ *   out[t,f] = sum over sorted rows r whose token is t (src_index[r] / k == t)
+ *              of gate_w[r] * y[r,f],
+ * in fp64.  y[T*k,F] holds the products of every sorted row (fp64),
+ * out[T,F] receives the result. */
+int mko_combine(const double* y, const int32_t* src_index, const float* gate_w,
+                int64_t T, int k, int F, double* out);
+
 /* Number of threads the oracle's parallel loops use. */
 int mko_num_threads(void);
 

@@ -37,7 +37,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mko_route.argtypes = [_p, _i64, _int, _int, _p, _p]
         lib.mko_dispatch.argtypes = [_p, _p, _i64, _int, _int, _p, _p, _p]
         lib.mko_expert_rows.argtypes = [_p, _p, _i64, _int, _int, _int, _int, _p, _p, _p, _i64, _p]
-        for f in (lib.mko_route, lib.mko_dispatch, lib.mko_expert_rows):
+        lib.mko_combine.argtypes = [_p, _p, _p, _i64, _int, _int, _p]
+        for f in (lib.mko_route, lib.mko_dispatch, lib.mko_expert_rows, lib.mko_combine):
             f.restype = _int
         lib.mko_num_threads.restype = _int
         _LIBS[path] = lib
@@ -95,6 +96,16 @@ class Oracle:
         _check(self.lib.mko_expert_rows(_ptr(x_bits), _ptr(W_bits), T, H, F, E, k, _ptr(offsets), _ptr(src),
                                         _ptr(rows), rows.size, _ptr(y)), "mko_expert_rows")
         return y
+
+    def combine(self, y, src, gate_w, T, k):
+        """fp64 out[T,F] from the products y[T*k,F] of every sorted row."""
+        y = np.ascontiguousarray(y, dtype=np.float64)
+        src = np.ascontiguousarray(src, dtype=np.int32)
+        gate_w = np.ascontiguousarray(gate_w, dtype=np.float32)
+        F = y.shape[1]
+        out = np.zeros((T, F), dtype=np.float64)
+        _check(self.lib.mko_combine(_ptr(y), _ptr(src), _ptr(gate_w), T, k, F, _ptr(out)), "mko_combine")
+        return out
 
     def full(self, x_bits, logits, W_bits, k, rows=None):
         """Every output of the path; ``rows`` limits the fp64 product to a sample."""

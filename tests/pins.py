@@ -257,6 +257,52 @@ def check_workload_invariants(o):
     assert len(np.unique(idx3)) < 80
 
 
+# --------------------------------------------------------------- combine ----
+
+def _oracle_combine(o, x, l, W, k):
+    out = o.full(x, l, W, k)
+    T = x.shape[0]
+    return out, o.combine(out["y"], out["src_index"], out["gate_w"], T, k)
+
+
+def check_combine_k1_is_the_row(o):
+    rng = np.random.default_rng(18)
+    T, H, F, E = 9, 8, 6, 4
+    x = _bf16(rng.standard_normal((T, H)))
+    W = _bf16(rng.standard_normal((E, H, F)))
+    out, comb = _oracle_combine(o, x, rng.standard_normal((T, E)).astype(np.float32), W, 1)
+    for r, q in enumerate(out["src_index"]):
+        assert np.array_equal(comb[q], out["y"][r])  # gate 1, one row per token
+
+
+def check_combine_shared_weights_is_dense(o):
+    """Every expert the same W0: the gates sum to 1, so out = x . W0."""
+    rng = np.random.default_rng(19)
+    T, H, F, E, k = 12, 10, 7, 5, 3
+    x = _bf16(rng.standard_normal((T, H)))
+    W0 = rng.standard_normal((H, F))
+    W = _bf16(np.repeat(W0[None], E, axis=0))
+    _, comb = _oracle_combine(o, x, rng.standard_normal((T, E)).astype(np.float32), W, k)
+    ref = np.matmul(synth.bf16_bits_to_f32(x).astype(np.float64), synth.bf16_bits_to_f32(W[0]).astype(np.float64))
+    assert np.allclose(comb, ref, rtol=1e-6, atol=1e-6)
+
+
+def check_combine_scaled_identity_experts(o):
+    """W[e] = c_e * I: out[t] = x[t] * sum_j gate[t,j] * c[idx[t,j]]."""
+    rng = np.random.default_rng(20)
+    T, H, E, k = 15, 6, 6, 3
+    c = np.array([1.0, -2.0, 0.5, 4.0, -0.25, 3.0])
+    W = _bf16(c[:, None, None] * np.eye(H)[None])
+    x = _bf16(rng.standard_normal((T, H)))
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    idx, gate = o.route(l, k)
+    _, comb = _oracle_combine(o, x, l, W, k)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    for t in range(T):
+        s = sum(float(gate[t, j]) * c[idx[t, j]] for j in range(k))
+        assert np.allclose(comb[t], xf[t] * s, rtol=1e-12, atol=1e-12), t
+
+
 ALL_CHECKS = [
     check_topk_bruteforce,
     check_topk_special_cases,
@@ -267,4 +313,7 @@ ALL_CHECKS = [
     check_gemm_one_hot_dense_loop,
     check_identity_weights,
     check_worked_example,
+    check_combine_k1_is_the_row,
+    check_combine_shared_weights_is_dense,
+    check_combine_scaled_identity_experts,
 ]

@@ -306,22 +306,29 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     cfg = mk.make_config(dispatch_ctas=args.dispatch_ctas, n_group=args.n_group)
 
-    def call(c):
-        st = mk.mk_moe_dispatch_gemm_ex(x, logits, w.T, w.H, w.E, w.k, W, w.F, out["y_sorted"], out["src_index"],
-                                        out["expert_offsets"], out["gate_w"], stream, c)
+    combined = torch.empty((w.T, w.F), dtype=torch.bfloat16, device=dev)
+
+    def call(c, combine=False):
+        if combine:
+            st = mk.mk_moe_dispatch_gemm_combine(x, logits, w.T, w.H, w.E, w.k, W, w.F, out["y_sorted"],
+                                                 out["src_index"], out["expert_offsets"], out["gate_w"], combined,
+                                                 stream, c)
+        else:
+            st = mk.mk_moe_dispatch_gemm_ex(x, logits, w.T, w.H, w.E, w.k, W, w.F, out["y_sorted"],
+                                            out["src_index"], out["expert_offsets"], out["gate_w"], stream, c)
         if st != mk.MK_OK:
             raise mk.MkError(st, "mk_moe_dispatch_gemm_ex")
 
-    def timed(c, steps, warmup):
+    def timed(c, steps, warmup, combine=False):
         for _ in range(warmup):
             flush.fill_(1)
-            call(c)
+            call(c, combine)
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in evs:
             flush.fill_(1)
             a.record(stream)
-            call(c)
+            call(c, combine)
             b.record(stream)
         torch.cuda.synchronize()
         st = mk.mk_get_status(stream)
@@ -384,6 +391,13 @@ def run_ours(args, w):
         ums = statistics.mean(timed(ucfg, min(args.steps, 50), 3))
         line["unfused"] = {"ms_per_step": ums, "tflops": w.flop / (ums / 1e3) / 1e12,
                            "fused_speedup": ums / ms_mean, "launches_per_step": 4}
+        # the MoE layer's combine (gated sum of each token's expert rows)
+        cms = statistics.mean(timed(cfg, min(args.steps, 50), 3, combine=True))
+        cums = statistics.mean(timed(ucfg, min(args.steps, 50), 3, combine=True))
+        cbytes = w.rows * w.F * 2 + w.T * w.F * 2 + w.rows * 8  # y_sorted read, out written, rows + gates
+        line["combine"] = {"fused_ms": cms, "unfused_ms": cums, "fused_speedup": cums / cms,
+                           "added_ms": cms - ms_mean, "bytes": cbytes,
+                           "added_gbs": cbytes / max(cms - ms_mean, 1e-6) * 1e3 / 1e9}
         # end to end through the host-buffer entry point
         xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
         lh = torch.from_numpy(l_np).pin_memory()

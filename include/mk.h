@@ -131,6 +131,22 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
                                     int32_t* expert_offsets, float* gate_w, void* stream,
                                     const mk_config_t* cfg, void* workspace, size_t ws_bytes);
 
+/* The path plus the combine that completes an MoE layer: after the expert
+ * products, out[t,:] = sum_j gate[t,j] * y_sorted[row of (t,j), :] (fp32,
+ * slots in order, no atomics), in y_sorted's dtype (bf16, or f32 with
+ * MK_OUT_F32).  The pages name the operation "MoE Dispatch+GEMM" and route
+ * each token to experts ("mKernel : une bibliotheque ...", lefilia.fr,
+ * para. 3); this weighted sum of a token's expert outputs is the textbook
+ * step that follows.  out[T,F]: device, caller-owned, 16-byte aligned.
+ * Fused mode combines inside the same persistent launch after a grid
+ * barrier; unfused mode adds a fifth launch.  y_sorted and the other outputs
+ * are written as by mk_moe_dispatch_gemm_ex.  Not valid with
+ * MK_MODE_DISPATCH_ONLY. */
+mk_status_t mk_moe_dispatch_gemm_combine(const void* x, const float* logits, int T, int H, int E, int k,
+                                         const void* W, int F, void* y_sorted, int32_t* src_index,
+                                         int32_t* expert_offsets, float* gate_w, void* out, void* stream,
+                                         const mk_config_t* cfg, void* workspace, size_t ws_bytes);
+
 /* End-to-end variant: x, logits and the four outputs are HOST buffers
  * (pinned memory gives asynchronous copies); W stays on the device (expert
  * weights are resident).  Copies the inputs in, runs the fused path, copies

@@ -40,6 +40,7 @@ ABI_FUNCTIONS = (
     "mk_config_default",
     "mk_moe_dispatch_gemm",
     "mk_moe_dispatch_gemm_ex",
+    "mk_moe_dispatch_gemm_combine",
     "mk_moe_dispatch_gemm_host",
     "mk_moe_dispatch_gemm_noalloc",
     "mk_workspace_size",
@@ -112,6 +113,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     h.mk_moe_dispatch_gemm.restype = _i
     h.mk_moe_dispatch_gemm_ex.argtypes = sig + [ctypes.POINTER(mk_config_t), _p, ctypes.c_size_t]
     h.mk_moe_dispatch_gemm_ex.restype = _i
+    h.mk_moe_dispatch_gemm_combine.argtypes = sig[:-1] + [_p, _p, ctypes.POINTER(mk_config_t), _p,
+                                                           ctypes.c_size_t]
+    h.mk_moe_dispatch_gemm_combine.restype = _i
     h.mk_moe_dispatch_gemm_host.argtypes = sig + [ctypes.POINTER(mk_config_t)]
     h.mk_moe_dispatch_gemm_host.restype = _i
     h.mk_moe_dispatch_gemm_noalloc.argtypes = sig + [ctypes.POINTER(mk_config_t)]
@@ -200,6 +204,31 @@ def mk_moe_dispatch_gemm_ex(x, logits, T, H, E, k, W, F, y_sorted, src_index, ex
                                              _ptr(src_index), _ptr(expert_offsets), _ptr(gate_w), _stream(stream),
                                              ctypes.byref(cfg) if cfg is not None else None, _ptr(workspace),
                                              int(ws_bytes)))
+
+
+def mk_moe_dispatch_gemm_combine(x, logits, T, H, E, k, W, F, y_sorted, src_index, expert_offsets, gate_w, out,
+                                 stream=None, cfg: mk_config_t | None = None, workspace=None, ws_bytes: int = 0) -> int:
+    return int(lib().mk_moe_dispatch_gemm_combine(_ptr(x), _ptr(logits), T, H, E, k, _ptr(W), F, _ptr(y_sorted),
+                                                  _ptr(src_index), _ptr(expert_offsets), _ptr(gate_w), _ptr(out),
+                                                  _stream(stream), ctypes.byref(cfg) if cfg is not None else None,
+                                                  _ptr(workspace), int(ws_bytes)))
+
+
+def moe_layer(x, logits, W, k, cfg: mk_config_t | None = None, stream=None, check=True):
+    """Dispatch + expert GEMM + combine on torch tensors; returns the outputs
+    of moe_dispatch_gemm plus ``out[T,F]``."""
+    import torch
+
+    T, H = x.shape
+    E, _, F = W.shape
+    o = alloc_outputs(T, F, E, k, cfg.out_dtype if cfg is not None else MK_OUT_BF16, x.device)
+    o["out"] = torch.empty((T, F), dtype=o["y_sorted"].dtype, device=x.device)
+    st = mk_moe_dispatch_gemm_combine(x, logits, T, H, E, k, W, F, o["y_sorted"], o["src_index"],
+                                      o["expert_offsets"], o["gate_w"], o["out"], stream, cfg)
+    _check(st, "mk_moe_dispatch_gemm_combine")
+    if check:
+        _check(mk_get_status(stream), "device status")
+    return o
 
 
 def mk_moe_dispatch_gemm_host(x_host, logits_host, T, H, E, k, W, F, y_host, src_host, offsets_host, gate_host,

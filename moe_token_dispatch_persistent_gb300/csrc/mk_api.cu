@@ -226,10 +226,15 @@ size_t mk_workspace_size(int T, int H, int F, int E, int k, const mk_config_t* c
     return ws_layout(T, H, E, k).total;
 }
 
-mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, int H, int E, int k, const void* W,
-                                    int F, void* y_sorted, int32_t* src_index, int32_t* expert_offsets,
-                                    float* gate_w, void* stream, const mk_config_t* cfg_in, void* workspace,
-                                    size_t ws_bytes) {
+}  // extern "C"
+
+namespace {
+
+// The whole path; with combine_out it also combines each token's expert
+// rows (gated sum) into combine_out[T,F].
+mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,
+                     void* y_sorted, int32_t* src_index, int32_t* expert_offsets, float* gate_w, void* combine_out,
+                     void* stream, const mk_config_t* cfg_in, void* workspace, size_t ws_bytes) {
     g_last_info = mk_launch_info_t{};
     mk_status_t s = validate_sizes(T, H, E, k, F);
     if (s != MK_OK) return s;
@@ -249,6 +254,7 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
             !aligned(gate_w, 4))
             return MK_ERR_INVALID_ARG;
         if (y_sorted && !aligned(y_sorted, 16)) return MK_ERR_INVALID_ARG;
+        if (combine_out && (!aligned(combine_out, 16) || c.mode == MK_MODE_DISPATCH_ONLY)) return MK_ERR_INVALID_ARG;
     }
     int dev = 0;
     DevInfo* d = nullptr;
@@ -324,6 +330,8 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
     p.topk_gate = reinterpret_cast<float*>(ws + L.topk_gate);
     p.lrank = reinterpret_cast<int32_t*>(ws + L.lrank);
     p.bases = reinterpret_cast<int32_t*>(ws + L.bases);
+    p.row_of = reinterpret_cast<int32_t*>(ws + L.row_of);
+    p.combine_out = combine_out;
     p.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
     p.xs = reinterpret_cast<uint16_t*>(ws + L.xs);
     p.trace_buf = reinterpret_cast<unsigned long long*>(ws + L.trace);
@@ -343,7 +351,7 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
     cudaError_t err;
     if (c.mode == MK_MODE_UNFUSED) {
         err = launch_unfused(p, tmA, tmB, grid, st);
-        g_last_info.launches = 4;
+        g_last_info.launches = combine_out ? 5 : 4;
     } else {
         err = launch_fused(p, tmA, tmB, grid, st);
         g_last_info.launches = 1;
@@ -357,6 +365,27 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
         fprintf(stderr, "[mk] T=%d H=%d F=%d E=%d k=%d mode=%d grid=%d dispatch=%d n_group=%d slots=%d ws=%zu\n", T, H,
                 F, E, k, c.mode, grid, p.dispatch_ctas, p.n_group, p.gather_slots, L.total);
     return err == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, int H, int E, int k, const void* W,
+                                    int F, void* y_sorted, int32_t* src_index, int32_t* expert_offsets,
+                                    float* gate_w, void* stream, const mk_config_t* cfg, void* workspace,
+                                    size_t ws_bytes) {
+    return run_path(x, logits, T, H, E, k, W, F, y_sorted, src_index, expert_offsets, gate_w, nullptr, stream, cfg,
+                    workspace, ws_bytes);
+}
+
+mk_status_t mk_moe_dispatch_gemm_combine(const void* x, const float* logits, int T, int H, int E, int k,
+                                         const void* W, int F, void* y_sorted, int32_t* src_index,
+                                         int32_t* expert_offsets, float* gate_w, void* out, void* stream,
+                                         const mk_config_t* cfg, void* workspace, size_t ws_bytes) {
+    if (T > 0 && !out) return MK_ERR_INVALID_ARG;
+    return run_path(x, logits, T, H, E, k, W, F, y_sorted, src_index, expert_offsets, gate_w, out, stream, cfg,
+                    workspace, ws_bytes);
 }
 
 mk_status_t mk_moe_dispatch_gemm(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,

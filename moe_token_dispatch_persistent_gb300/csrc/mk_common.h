@@ -71,7 +71,8 @@ struct Ctl {
     uint32_t next_item;      // GEMM work queue (compute role)
     uint32_t abort;          // 1 once any CTA of this call gave up
     uint32_t tiles_done;     // tiles the dispatch role has gathered and flagged
-    uint32_t pad[56];
+    uint32_t bar_computed;   // CTAs done with the GEMM (combine barrier)
+    uint32_t pad[55];
 };
 static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");
 
@@ -92,6 +93,7 @@ enum Site : int {
     SITE_DEST_RANGE = 11,
     SITE_ROW_TOTAL = 12,
     SITE_DRAIN = 13,
+    SITE_BAR_COMPUTED = 14,
 };
 
 enum ErrCode : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_FAULT = 2 };
@@ -130,6 +132,8 @@ struct Params {
     float* topk_gate;        // [T*k]
     int32_t* lrank;          // [T*k]
     int32_t* bases;          // [nch][E] (unfused path)
+    int32_t* row_of;         // [T*k] sorted row of each (t, j)
+    void* combine_out;       // [T,F] (y_sorted's dtype) or null: no combine
     uint32_t* ready;         // [max_tiles]
     uint16_t* xs;            // [T*k,H] bf16 staging
     unsigned long long* trace_buf;  // [grid][TRACE_SLOTS]
@@ -138,7 +142,7 @@ struct Params {
 
 // Workspace carve-up, shared by the size query and the launcher.
 struct WsLayout {
-    size_t ctl, counts, topk_idx, topk_gate, lrank, bases, ready, trace, xs, total;
+    size_t ctl, counts, topk_idx, topk_gate, lrank, row_of, bases, ready, trace, xs, total;
 };
 
 inline size_t ws_align(size_t v) { return (v + 255) & ~size_t(255); }
@@ -156,6 +160,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int grid = MAX_GRID) {
     L.topk_idx = o;   o = ws_align(o + rows * 4);
     L.topk_gate = o;  o = ws_align(o + rows * 4);
     L.lrank = o;      o = ws_align(o + rows * 4);
+    L.row_of = o;     o = ws_align(o + rows * 4);
     L.bases = o;      o = ws_align(o + nch * E * 4);
     L.ready = o;      o = ws_align(o + max_tiles * 4);
     L.trace = o;      o = ws_align(o + size_t(grid) * TRACE_SLOTS * 8);

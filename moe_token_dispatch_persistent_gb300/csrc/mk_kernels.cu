@@ -436,6 +436,7 @@ __device__ void scatter_chunk(const Params& p, int c, const int* cbase, const Wa
             }
             p.src_index[dest] = q;
             p.gate_w[dest] = g[u];
+            p.row_of[q] = dest;
         }
     }
 }
@@ -538,6 +539,7 @@ __device__ void push_gather_chunk(const Params& p, int c, CtrlSmem* cs, uint32_t
             }
             p.src_index[dest] = q;
             p.gate_w[dest] = __ldcg(p.topk_gate + q);
+            p.row_of[q] = dest;
             bulk_wait_read<0>();
             mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
             bulk_load(slot, p.x + size_t(q / k) * p.H, row_bytes, &cs->gbar[lane]);
@@ -786,6 +788,79 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             mbar_arrive(&cs->acc_empty[acc]);
             acc ^= 1u;
             if (acc == 0) accph ^= 1u;
+        }
+    }
+}
+
+// ------------------------------------------------------------ combine ------
+
+// out[t,:] = sum_j gate[t,j] * y_sorted[row_of(t,j), :], fp32 in slot order
+// (deterministic, no atomics), stored in y_sorted's dtype.  Tokens are
+// spread over CTAs [first, first + stride, ...); each thread owns 16-byte
+// column chunks, two in flight.
+__device__ void combine_tokens(const Params& p, int first, int stride) {
+    const int k = p.k, F = p.F;
+    const int nchunk = F / 8;  // 8 values per chunk (16 B of bf16, 32 B of f32)
+    for (int t = first; t < p.T; t += stride) {
+        int r[MAX_K];
+        float g[MAX_K];
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
+            // in range even if an error path left a row unrecorded
+            r[j] = j < k ? min(max(__ldcg(p.row_of + size_t(t) * k + j), 0), p.rows - 1) : 0;
+            g[j] = j < k ? __ldcg(p.topk_gate + size_t(t) * k + j) : 0.f;
+        }
+        for (int c0 = threadIdx.x; c0 < nchunk; c0 += 2 * NTHREADS) {
+            float acc[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int v = 0; v < 8; ++v) acc[u][v] = 0.f;
+#pragma unroll
+            for (int j = 0; j < MAX_K; ++j) {
+                if (j >= k) break;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int c = c0 + u * NTHREADS;
+                    if (c >= nchunk) continue;
+                    if (p.out_f32) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            static_cast<const float*>(p.y) + size_t(r[j]) * F + size_t(c) * 8);
+                        const float4 a = __ldcg(src), b = __ldcg(src + 1);
+                        acc[u][0] += g[j] * a.x; acc[u][1] += g[j] * a.y; acc[u][2] += g[j] * a.z; acc[u][3] += g[j] * a.w;
+                        acc[u][4] += g[j] * b.x; acc[u][5] += g[j] * b.y; acc[u][6] += g[j] * b.z; acc[u][7] += g[j] * b.w;
+                    } else {
+                        const uint4 q = __ldcg(reinterpret_cast<const uint4*>(
+                            static_cast<const uint16_t*>(p.y) + size_t(r[j]) * F + size_t(c) * 8));
+                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[v]));
+                            acc[u][2 * v] += g[j] * f.x;
+                            acc[u][2 * v + 1] += g[j] * f.y;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int c = c0 + u * NTHREADS;
+                if (c >= nchunk) continue;
+                if (p.out_f32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.combine_out) + size_t(t) * F + size_t(c) * 8);
+                    dst[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+                    dst[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
+                } else {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[u][2 * v], acc[u][2 * v + 1]);
+                        pk[v] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.combine_out) + size_t(t) * F + size_t(c) * 8) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
         }
     }
 }
@@ -1078,6 +1153,7 @@ __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
             c->next_tile = 0;
             c->next_item = 0;
             c->tiles_done = 0;
+            c->bar_computed = 0;
             c->abort = 0;
             c->epoch = c->epoch + 1u;  // calls completed on this workspace
             c->exit_count = 0;
@@ -1158,6 +1234,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             stamp(p, 7);
         }
     }
+    if (p.combine_out) {
+        // every CTA's expert rows are written before any token is combined
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atom_add_acq_rel_u32(&p.ctl->bar_computed, 1u);
+            cs->bcast[3] = ok && !aborted(w) && wait_geq(&p.ctl->bar_computed, gridDim.x, w, SITE_BAR_COMPUTED);
+        }
+        __syncthreads();
+        stamp(p, 8);
+        if (cs->bcast[3]) combine_tokens(p, blockIdx.x, gridDim.x);
+        stamp(p, 9);
+    }
     cta_teardown<PAIR>(p, cs, p.compute != 0);
 }
 
@@ -1200,6 +1289,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_gather_kernel(const Params p) 
     const WaitCtx w{nullptr, 0u, p.spin_limit_ns};
     uint32_t ph = 0;
     push_gather_chunk(p, blockIdx.x, cs, ph, w);
+}
+
+// Unfused baseline, launch 5 (with a combine): tokens over the grid.
+__global__ void __launch_bounds__(NTHREADS, 1) mk_combine_kernel(const Params p) {
+    combine_tokens(p, blockIdx.x, gridDim.x);
 }
 
 // Unfused baseline, launch 4: persistent expert GEMM over all tiles.
@@ -1270,6 +1364,8 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (!p.pair) {
         mk_gemm_kernel<0><<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b);
+        if ((err = cudaGetLastError()) != cudaSuccess || !p.combine_out) return err;
+        mk_combine_kernel<<<grid, NTHREADS, 0, st>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg{};
@@ -1284,7 +1380,9 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b);
+    if ((err = cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b)) != cudaSuccess || !p.combine_out) return err;
+    mk_combine_kernel<<<grid, NTHREADS, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t set_kernel_attributes() {

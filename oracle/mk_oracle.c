@@ -116,6 +116,48 @@ int mko_dispatch(const int32_t* topk_idx, const float* topk_gate,
     return MKO_OK;
 }
 
+int mko_gated_rows(const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                   int64_t T, int H, int F, int E, int k,
+                   const int32_t* expert_offsets, const int32_t* src_index,
+                   const int64_t* rows, int64_t n, double* y) {
+    if (T < 0 || H < 1 || F < 1 || E < 1 || k < 1 || n < 0) return MKO_EARG;
+    if (n > 0 && (!x || !W1 || !W3 || !expert_offsets || !src_index || !rows || !y)) return MKO_EARG;
+    const int64_t nrows = T * (int64_t)k;
+    for (int64_t i = 0; i < n; ++i)
+        if (rows[i] < 0 || rows[i] >= nrows) return MKO_EARG;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(|: bad)
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = rows[i];
+        int e = 0;
+        while (!(expert_offsets[e] <= r && r < expert_offsets[e + 1])) ++e;
+        const int64_t t = src_index[r] / k;
+        const uint16_t* xt = x + t * (int64_t)H;
+        const uint16_t* W1e = W1 + (int64_t)e * H * F;
+        const uint16_t* W3e = W3 + (int64_t)e * H * F;
+        double* a = (double*)calloc((size_t)F, sizeof(double));
+        double* b = (double*)calloc((size_t)F, sizeof(double));
+        if (!a || !b) {
+            free(a);
+            free(b);
+            bad = 1;
+            continue;
+        }
+        for (int h = 0; h < H; ++h) {
+            const double xv = bf16_to_double(xt[h]);
+            for (int f = 0; f < F; ++f) {
+                a[f] += xv * bf16_to_double(W1e[(int64_t)h * F + f]);
+                b[f] += xv * bf16_to_double(W3e[(int64_t)h * F + f]);
+            }
+        }
+        double* yr = y + i * (int64_t)F;
+        for (int f = 0; f < F; ++f) yr[f] = a[f] / (1.0 + exp(-a[f])) * b[f];
+        free(a);
+        free(b);
+    }
+    return bad ? MKO_EARG : MKO_OK;
+}
+
 int mko_combine(const double* y, const int32_t* src_index, const float* gate_w,
                 int64_t T, int k, int F, double* out) {
     if (T < 0 || k < 1 || F < 1) return MKO_EARG;

@@ -71,6 +71,16 @@ int mko_expert_rows(const uint16_t* x, const uint16_t* W,
 int mko_combine(const double* y, const int32_t* src_index, const float* gate_w,
                 int64_t T, int k, int F, double* out);
 
+/* Gated expert FFN (SwiGLU) for a list of sorted rows: with the row's token t
+ * and expert e,
+ *   a[f] = sum_h x[t,h] * W1[e,h,f],  b[f] = sum_h x[t,h] * W3[e,h,f]  (fp64,
+ *   ascending h),   h[r,f] = silu(a[f]) * b[f],  silu(z) = z / (1 + exp(-z)).
+ * Layouts and `rows` as for mko_expert_rows; y[n,F] receives h. */
+int mko_gated_rows(const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                   int64_t T, int H, int F, int E, int k,
+                   const int32_t* expert_offsets, const int32_t* src_index,
+                   const int64_t* rows, int64_t n, double* y);
+
 /* Number of threads the oracle's parallel loops use. */
 int mko_num_threads(void);
 

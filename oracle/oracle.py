@@ -38,7 +38,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mko_dispatch.argtypes = [_p, _p, _i64, _int, _int, _p, _p, _p]
         lib.mko_expert_rows.argtypes = [_p, _p, _i64, _int, _int, _int, _int, _p, _p, _p, _i64, _p]
         lib.mko_combine.argtypes = [_p, _p, _p, _i64, _int, _int, _p]
-        for f in (lib.mko_route, lib.mko_dispatch, lib.mko_expert_rows, lib.mko_combine):
+        lib.mko_gated_rows.argtypes = [_p, _p, _p, _i64, _int, _int, _int, _int, _p, _p, _p, _i64, _p]
+        for f in (lib.mko_route, lib.mko_dispatch, lib.mko_expert_rows, lib.mko_combine, lib.mko_gated_rows):
             f.restype = _int
         lib.mko_num_threads.restype = _int
         _LIBS[path] = lib
@@ -96,6 +97,29 @@ class Oracle:
         _check(self.lib.mko_expert_rows(_ptr(x_bits), _ptr(W_bits), T, H, F, E, k, _ptr(offsets), _ptr(src),
                                         _ptr(rows), rows.size, _ptr(y)), "mko_expert_rows")
         return y
+
+    def gated_rows(self, x_bits, W1_bits, W3_bits, k, offsets, src, rows):
+        """fp64 silu(x.W1) * (x.W3) for the sorted rows ``rows``."""
+        x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        W1_bits = np.ascontiguousarray(W1_bits, dtype=np.uint16)
+        W3_bits = np.ascontiguousarray(W3_bits, dtype=np.uint16)
+        T, H = x_bits.shape
+        E, H2, F = W1_bits.shape
+        assert H2 == H and W3_bits.shape == W1_bits.shape
+        offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+        src = np.ascontiguousarray(src, dtype=np.int32)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        y = np.zeros((rows.size, F), dtype=np.float64)
+        _check(self.lib.mko_gated_rows(_ptr(x_bits), _ptr(W1_bits), _ptr(W3_bits), T, H, F, E, k, _ptr(offsets),
+                                       _ptr(src), _ptr(rows), rows.size, _ptr(y)), "mko_gated_rows")
+        return y
+
+    def gated_full(self, x_bits, logits, W1_bits, W3_bits, k):
+        E = W1_bits.shape[0]
+        idx, gate = self.route(logits, k)
+        offsets, src, gw = self.dispatch(idx, gate, E)
+        y = self.gated_rows(x_bits, W1_bits, W3_bits, k, offsets, src, np.arange(src.size))
+        return dict(topk_idx=idx, topk_gate=gate, expert_offsets=offsets, src_index=src, gate_w=gw, y=y)
 
     def combine(self, y, src, gate_w, T, k):
         """fp64 out[T,F] from the products y[T*k,F] of every sorted row."""

@@ -303,6 +303,55 @@ def check_combine_scaled_identity_experts(o):
         assert np.allclose(comb[t], xf[t] * s, rtol=1e-12, atol=1e-12), t
 
 
+# ------------------------------------------------------------ gated FFN ----
+
+def check_gated_vs_numpy(o):
+    """silu(x.W1) * (x.W3) with numpy matmuls and silu(z) = z * (1 + tanh(z/2)) / 2."""
+    rng = np.random.default_rng(21)
+    for (T, H, F, E, k) in [(6, 8, 5, 3, 2), (10, 12, 9, 4, 3)]:
+        x = _bf16(rng.standard_normal((T, H)))
+        W1 = _bf16(2.0 * rng.standard_normal((E, H, F)))
+        W3 = _bf16(rng.standard_normal((E, H, F)))
+        l = rng.standard_normal((T, E)).astype(np.float32)
+        out = o.gated_full(x, l, W1, W3, k)
+        xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+        W1f = synth.bf16_bits_to_f32(W1).astype(np.float64)
+        W3f = synth.bf16_bits_to_f32(W3).astype(np.float64)
+        off, src = out["expert_offsets"], out["src_index"]
+        for r in range(T * k):
+            e = int(np.searchsorted(off, r, side="right") - 1)
+            a = np.matmul(xf[src[r] // k], W1f[e])
+            b = np.matmul(xf[src[r] // k], W3f[e])
+            ref = a * (1.0 + np.tanh(a / 2.0)) / 2.0 * b
+            assert np.allclose(out["y"][r], ref, rtol=1e-11, atol=1e-12), (T, r)
+
+
+def check_gated_zero_gate_projection(o):
+    rng = np.random.default_rng(22)
+    T, H, F, E, k = 8, 6, 4, 3, 2
+    x = _bf16(rng.standard_normal((T, H)))
+    W1 = _bf16(np.zeros((E, H, F)))
+    W3 = _bf16(rng.standard_normal((E, H, F)))
+    out = o.gated_full(x, rng.standard_normal((T, E)).astype(np.float32), W1, W3, k)
+    assert (out["y"] == 0).all()
+
+
+def check_gated_odd_part(o):
+    """One-hot routing to W1 = +I or -I with W3 = I: silu(z) - silu(-z) = z,
+    so the two rows of a token differ by x**2."""
+    rng = np.random.default_rng(23)
+    T, H = 10, 6
+    x = _bf16(rng.standard_normal((T, H)))
+    eye = np.eye(H)
+    W1 = _bf16(np.stack([eye, -eye]))
+    W3 = _bf16(np.stack([eye, eye]))
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    hp = o.gated_full(x, np.tile(np.array([[5.0, 0.0]], np.float32), (T, 1)), W1, W3, 1)
+    hm = o.gated_full(x, np.tile(np.array([[0.0, 5.0]], np.float32), (T, 1)), W1, W3, 1)
+    # one expert per call: sorted rows are the tokens in order
+    assert np.allclose(hp["y"] - hm["y"], xf * xf, rtol=1e-13, atol=1e-15)
+
+
 ALL_CHECKS = [
     check_topk_bruteforce,
     check_topk_special_cases,
@@ -316,4 +365,7 @@ ALL_CHECKS = [
     check_combine_k1_is_the_row,
     check_combine_shared_weights_is_dense,
     check_combine_scaled_identity_experts,
+    check_gated_vs_numpy,
+    check_gated_zero_gate_projection,
+    check_gated_odd_part,
 ]

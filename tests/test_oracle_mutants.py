@@ -33,14 +33,19 @@ MUTANTS = {
     "src_index_slot_major": ("src_index[r] = (int32_t)(t * k + j);", "src_index[r] = (int32_t)(j * T + t);"),
     "gate_w_token_order": ("gate_w[r] = topk_gate[t * k + j];", "gate_w[r] = topk_gate[r];"),
     "transposed_w": ("yr[f] += xv * bf16_to_double(wrow[f]);", "yr[f] += xv * bf16_to_double(We[(int64_t)f * H + h]);"),
-    "wrong_token": ("const int64_t t = src_index[r] / k;\n        const uint16_t* xt",
-                    "const int64_t t = r / k;\n        const uint16_t* xt"),
-    "dropped_first_h": ("for (int h = 0; h < H; ++h) {", "for (int h = 1; h < H; ++h) {"),
+    "wrong_token": ("const int64_t t = src_index[r] / k;\n        const uint16_t* xt = x + t * (int64_t)H;\n        const uint16_t* We",
+                    "const int64_t t = r / k;\n        const uint16_t* xt = x + t * (int64_t)H;\n        const uint16_t* We"),
+    "dropped_first_h": ("for (int h = 0; h < H; ++h) {\n            const double xv = bf16_to_double(xt[h]);\n            const uint16_t* wrow",
+                        "for (int h = 1; h < H; ++h) {\n            const double xv = bf16_to_double(xt[h]);\n            const uint16_t* wrow"),
     "wrong_expert_weights": ("const uint16_t* We = W + (int64_t)e * H * F;", "const uint16_t* We = W;"),
     "bf16_decode_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
     "combine_wrong_token": ("const int64_t t = src_index[r] / k;\n        const double g", "const int64_t t = src_index[r] % k;\n        const double g"),
     "combine_ignores_gate": ("const double g = (double)gate_w[r];", "const double g = 1.0;"),
     "combine_overwrites": ("out[t * F + f] += g * y[r * F + f];", "out[t * F + f] = g * y[r * F + f];"),
+    "gated_exp_sign": ("yr[f] = a[f] / (1.0 + exp(-a[f])) * b[f];", "yr[f] = a[f] / (1.0 + exp(a[f])) * b[f];"),
+    "gated_swapped_projections": ("yr[f] = a[f] / (1.0 + exp(-a[f])) * b[f];", "yr[f] = b[f] / (1.0 + exp(-b[f])) * a[f];"),
+    "gated_no_up_projection": ("yr[f] = a[f] / (1.0 + exp(-a[f])) * b[f];", "yr[f] = a[f] / (1.0 + exp(-a[f]));"),
+    "gated_w3_is_w1": ("const uint16_t* W3e = W3 + (int64_t)e * H * F;", "const uint16_t* W3e = W1 + (int64_t)e * H * F;"),
     "combine_uniform_gate": ("const double g = (double)gate_w[r];", "const double g = 1.0 / k;"),
 }
 

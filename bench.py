@@ -398,6 +398,34 @@ def run_ours(args, w):
         line["combine"] = {"fused_ms": cms, "unfused_ms": cums, "fused_speedup": cums / cms,
                            "added_ms": cms - ms_mean, "bytes": cbytes,
                            "added_gbs": cbytes / max(cms - ms_mean, 1e-6) * 1e3 / 1e9}
+        # the gated (SwiGLU) expert FFN: two projections, one tensor-core pass per item
+        w3 = synth.Workload(w.name, w.T, w.H, w.F, w.E, w.k, w.seed + 7, w.kind)
+        W3 = torch.from_numpy(synth.make_w(w3).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        def gated_once():
+            st = mk.mk_moe_dispatch_gated(x, logits, w.T, w.H, w.E, w.k, W, W3, w.F, out["y_sorted"],
+                                          out["src_index"], out["expert_offsets"], out["gate_w"], stream, cfg)
+            if st != mk.MK_OK:
+                raise mk.MkError(st, "mk_moe_dispatch_gated")
+
+        for _ in range(3):
+            flush.fill_(1)
+            gated_once()
+        gms_list = []
+        for _ in range(min(args.steps, 50)):
+            flush.fill_(1)
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            gated_once()
+            b_ev.record(stream)
+            gms_list.append((a_ev, b_ev))
+        torch.cuda.synchronize()
+        if mk.mk_get_status(stream) != mk.MK_OK:
+            raise RuntimeError("gated path: device error")
+        gms = statistics.mean(a.elapsed_time(b) for a, b in gms_list)
+        line["gated"] = {"ms": gms, "tflops": 2 * w.flop / (gms / 1e3) / 1e12,
+                         "frac_bf16": 2 * w.flop / (gms / 1e3) / 1e12 / peak}
+        del W3
         # end to end through the host-buffer entry point
         xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
         lh = torch.from_numpy(l_np).pin_memory()

@@ -147,6 +147,22 @@ mk_status_t mk_moe_dispatch_gemm_combine(const void* x, const float* logits, int
                                          int32_t* expert_offsets, float* gate_w, void* out, void* stream,
                                          const mk_config_t* cfg, void* workspace, size_t ws_bytes);
 
+/* Gated expert FFN (SwiGLU, the Mixtral / DeepSeek expert shape; both model
+ * families are named in "mKernel : une bibliotheque de noyaux fusionnes
+ * ...", lefilia.fr, para. 3): the same dispatch, then for sorted row r of
+ * token t routed to expert e,
+ *   h_sorted[r,:] = silu(x[t,:] . W1[e]) * (x[t,:] . W3[e]),  silu(a) = a / (1 + e^-a),
+ * both products accumulated in fp32 in the same tensor-core pass (the A tile
+ * is shared; 128 columns of each projection per work item) and the SwiGLU
+ * applied in the epilogue (fp32 expf) before rounding to bf16 (or f32 with
+ * MK_OUT_F32).  W1, W3: [E,H,F] bf16, device, 16-byte aligned.  Runs on
+ * single-SM tiles (MK_MMA_PAIR returns MK_ERR_UNSUPPORTED).  Other
+ * arguments and outputs as for mk_moe_dispatch_gemm_ex. */
+mk_status_t mk_moe_dispatch_gated(const void* x, const float* logits, int T, int H, int E, int k, const void* W1,
+                                  const void* W3, int F, void* h_sorted, int32_t* src_index,
+                                  int32_t* expert_offsets, float* gate_w, void* stream, const mk_config_t* cfg,
+                                  void* workspace, size_t ws_bytes);
+
 /* End-to-end variant: x, logits and the four outputs are HOST buffers
  * (pinned memory gives asynchronous copies); W stays on the device (expert
  * weights are resident).  Copies the inputs in, runs the fused path, copies

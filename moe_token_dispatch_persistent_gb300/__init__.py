@@ -41,6 +41,7 @@ ABI_FUNCTIONS = (
     "mk_moe_dispatch_gemm",
     "mk_moe_dispatch_gemm_ex",
     "mk_moe_dispatch_gemm_combine",
+    "mk_moe_dispatch_gated",
     "mk_moe_dispatch_gemm_host",
     "mk_moe_dispatch_gemm_noalloc",
     "mk_workspace_size",
@@ -116,6 +117,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     h.mk_moe_dispatch_gemm_combine.argtypes = sig[:-1] + [_p, _p, ctypes.POINTER(mk_config_t), _p,
                                                            ctypes.c_size_t]
     h.mk_moe_dispatch_gemm_combine.restype = _i
+    h.mk_moe_dispatch_gated.argtypes = [_p, _p, _i, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p,
+                                        ctypes.POINTER(mk_config_t), _p, ctypes.c_size_t]
+    h.mk_moe_dispatch_gated.restype = _i
     h.mk_moe_dispatch_gemm_host.argtypes = sig + [ctypes.POINTER(mk_config_t)]
     h.mk_moe_dispatch_gemm_host.restype = _i
     h.mk_moe_dispatch_gemm_noalloc.argtypes = sig + [ctypes.POINTER(mk_config_t)]
@@ -212,6 +216,27 @@ def mk_moe_dispatch_gemm_combine(x, logits, T, H, E, k, W, F, y_sorted, src_inde
                                                   _ptr(src_index), _ptr(expert_offsets), _ptr(gate_w), _ptr(out),
                                                   _stream(stream), ctypes.byref(cfg) if cfg is not None else None,
                                                   _ptr(workspace), int(ws_bytes)))
+
+
+def mk_moe_dispatch_gated(x, logits, T, H, E, k, W1, W3, F, h_sorted, src_index, expert_offsets, gate_w,
+                          stream=None, cfg: mk_config_t | None = None, workspace=None, ws_bytes: int = 0) -> int:
+    return int(lib().mk_moe_dispatch_gated(_ptr(x), _ptr(logits), T, H, E, k, _ptr(W1), _ptr(W3), F, _ptr(h_sorted),
+                                           _ptr(src_index), _ptr(expert_offsets), _ptr(gate_w), _stream(stream),
+                                           ctypes.byref(cfg) if cfg is not None else None, _ptr(workspace),
+                                           int(ws_bytes)))
+
+
+def moe_gated(x, logits, W1, W3, k, cfg: mk_config_t | None = None, stream=None, check=True):
+    """Dispatch + gated expert FFN on torch tensors; ``y_sorted`` holds h."""
+    T, H = x.shape
+    E, _, F = W1.shape
+    o = alloc_outputs(T, F, E, k, cfg.out_dtype if cfg is not None else MK_OUT_BF16, x.device)
+    st = mk_moe_dispatch_gated(x, logits, T, H, E, k, W1, W3, F, o["y_sorted"], o["src_index"],
+                               o["expert_offsets"], o["gate_w"], stream, cfg)
+    _check(st, "mk_moe_dispatch_gated")
+    if check:
+        _check(mk_get_status(stream), "device status")
+    return o
 
 
 def moe_layer(x, logits, W, k, cfg: mk_config_t | None = None, stream=None, check=True):

@@ -23,8 +23,10 @@
 #include "mk_common.h"
 
 namespace mk {
-cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st);
-cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st);
+cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, int grid,
+                         cudaStream_t st);
+cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                           int grid, cudaStream_t st);
 cudaError_t set_kernel_attributes();
 cudaError_t fused_max_blocks_per_sm(int* n);
 cudaError_t read_and_clear_error(uint32_t out[4], cudaStream_t st);
@@ -232,9 +234,9 @@ namespace {
 
 // The whole path; with combine_out it also combines each token's expert
 // rows (gated sum) into combine_out[T,F].
-mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,
-                     void* y_sorted, int32_t* src_index, int32_t* expert_offsets, float* gate_w, void* combine_out,
-                     void* stream, const mk_config_t* cfg_in, void* workspace, size_t ws_bytes) {
+mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, int k, const void* W, const void* W3,
+                     int F, void* y_sorted, int32_t* src_index, int32_t* expert_offsets, float* gate_w,
+                     void* combine_out, void* stream, const mk_config_t* cfg_in, void* workspace, size_t ws_bytes) {
     g_last_info = mk_launch_info_t{};
     mk_status_t s = validate_sizes(T, H, E, k, F);
     if (s != MK_OK) return s;
@@ -255,6 +257,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
             return MK_ERR_INVALID_ARG;
         if (y_sorted && !aligned(y_sorted, 16)) return MK_ERR_INVALID_ARG;
         if (combine_out && (!aligned(combine_out, 16) || c.mode == MK_MODE_DISPATCH_ONLY)) return MK_ERR_INVALID_ARG;
+        if (W3 && !aligned(W3, 16)) return MK_ERR_INVALID_ARG;
     }
     int dev = 0;
     DevInfo* d = nullptr;
@@ -267,6 +270,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     }
 
     const bool pair = resolve_pair(c, T, E, k) == MK_MMA_PAIR;
+    if (pair && W3) return MK_ERR_UNSUPPORTED;  // the gated FFN runs on single-SM tiles
     int grid = grid_for(*d, c);
     if (pair) grid &= ~1;  // whole clusters of two
     if (grid < (pair ? 2 : 1)) return MK_ERR_UNSUPPORTED;
@@ -299,7 +303,10 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.out_f32 = c.out_dtype == MK_OUT_F32;
     p.rows = rows;
     p.nch = nch;
-    p.nb = (F + BN - 1) / BN;
+    p.gated = W3 ? 1 : 0;
+    p.W3 = static_cast<const uint16_t*>(W3);
+    const int bnw = W3 ? BN / 2 : BN;  // gated: 128 columns of each projection per item
+    p.nb = (F + bnw - 1) / bnw;
     p.kblocks = H / BK;
     p.n_group = c.n_group > 0 ? (c.n_group < p.nb ? c.n_group : p.nb) : n_group_for(H, F, p.nb);
     p.mode = c.mode;
@@ -344,16 +351,19 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
         return MK_ERR_CUDA;
     if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
+    CUtensorMap tmB3 = tmB;
+    if (W3 && encode_2d(&tmB3, W3, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+        return MK_ERR_CUDA;
 
     if (p.trace && cudaMemsetAsync(p.trace_buf, 0, size_t(grid) * TRACE_SLOTS * 8, st) != cudaSuccess)
         return MK_ERR_CUDA;
 
     cudaError_t err;
     if (c.mode == MK_MODE_UNFUSED) {
-        err = launch_unfused(p, tmA, tmB, grid, st);
+        err = launch_unfused(p, tmA, tmB, tmB3, grid, st);
         g_last_info.launches = combine_out ? 5 : 4;
     } else {
-        err = launch_fused(p, tmA, tmB, grid, st);
+        err = launch_fused(p, tmA, tmB, tmB3, grid, st);
         g_last_info.launches = 1;
     }
     g_last_info.grid_ctas = grid;
@@ -375,8 +385,17 @@ mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, i
                                     int F, void* y_sorted, int32_t* src_index, int32_t* expert_offsets,
                                     float* gate_w, void* stream, const mk_config_t* cfg, void* workspace,
                                     size_t ws_bytes) {
-    return run_path(x, logits, T, H, E, k, W, F, y_sorted, src_index, expert_offsets, gate_w, nullptr, stream, cfg,
-                    workspace, ws_bytes);
+    return run_path(x, logits, T, H, E, k, W, nullptr, F, y_sorted, src_index, expert_offsets, gate_w, nullptr,
+                    stream, cfg, workspace, ws_bytes);
+}
+
+mk_status_t mk_moe_dispatch_gated(const void* x, const float* logits, int T, int H, int E, int k, const void* W1,
+                                  const void* W3, int F, void* h_sorted, int32_t* src_index, int32_t* expert_offsets,
+                                  float* gate_w, void* stream, const mk_config_t* cfg, void* workspace,
+                                  size_t ws_bytes) {
+    if (T > 0 && !W3) return MK_ERR_INVALID_ARG;
+    return run_path(x, logits, T, H, E, k, W1, T > 0 ? W3 : nullptr, F, h_sorted, src_index, expert_offsets, gate_w,
+                    nullptr, stream, cfg, workspace, ws_bytes);
 }
 
 mk_status_t mk_moe_dispatch_gemm_combine(const void* x, const float* logits, int T, int H, int E, int k,
@@ -384,8 +403,8 @@ mk_status_t mk_moe_dispatch_gemm_combine(const void* x, const float* logits, int
                                          int32_t* expert_offsets, float* gate_w, void* out, void* stream,
                                          const mk_config_t* cfg, void* workspace, size_t ws_bytes) {
     if (T > 0 && !out) return MK_ERR_INVALID_ARG;
-    return run_path(x, logits, T, H, E, k, W, F, y_sorted, src_index, expert_offsets, gate_w, out, stream, cfg,
-                    workspace, ws_bytes);
+    return run_path(x, logits, T, H, E, k, W, nullptr, F, y_sorted, src_index, expert_offsets, gate_w, out, stream,
+                    cfg, workspace, ws_bytes);
 }
 
 mk_status_t mk_moe_dispatch_gemm(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,

@@ -102,7 +102,8 @@ struct Params {
     // problem (device pointers)
     const uint16_t* x;       // [T,H] bf16
     const float* logits;     // [T,E]
-    const uint16_t* W;       // [E,H,F] bf16
+    const uint16_t* W;       // [E,H,F] bf16 (the gate projection W1 when gated)
+    const uint16_t* W3;      // [E,H,F] bf16 up projection (gated only)
     void* y;                 // [T*k,F] bf16 or f32
     int32_t* src_index;      // [T*k]
     int32_t* expert_offsets; // [E+1]
@@ -122,6 +123,7 @@ struct Params {
     int debug_drop_tile;     // tile whose flag is withheld (-1: none)
     int l2_prefetch;         // W k-blocks prefetched into L2 ahead of the TMA loads (0: off)
     int pair;                // 1: 2-SM MMA (cluster of 2 CTAs per 256-row tile)
+    int gated;               // 1: y = silu(x.W1) * (x.W3), 128-column N-blocks
     int tile_rows;           // rows per tile: 128, or 256 with pair
     int trace;
     long long spin_limit_ns;

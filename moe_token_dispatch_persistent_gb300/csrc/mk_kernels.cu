@@ -585,10 +585,37 @@ __device__ __forceinline__ void decode_item(const Params& p, const CtrlSmem* cs,
 }
 
 constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+// Gated FFN: two N = 128 products (gate W1, up W3) per item share the A tile.
+constexpr int GATED_BN = BN / 2;
+constexpr uint32_t IDESC_GATED = umma_idesc_bf16(BM, GATED_BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+
+// One thread's 32 consecutive fp32 results of row `row`, columns [col, col+32),
+// stored as bf16 (round to nearest even) or f32.
+__device__ __forceinline__ void store_row32(const Params& p, size_t row, int col, const uint32_t (&r)[32]) {
+    if (p.out_f32) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.y) + row * p.F + col);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + row * p.F + col);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const __nv_bfloat162 h =
+                    __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * u]), __uint_as_float(r[8 * v + 2 * u + 1]));
+                pk[u] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+}
 
 // Warp-specialised expert GEMM over work items (tile, N-block) taken from the
 // shared queue until it is empty.  wait_ready: spin on the tile's flag first.
-__device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, CtrlSmem* cs,
+__device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmB3,
+                             CtrlSmem* cs,
                              bool wait_ready, uint32_t flag, const WaitCtx& w) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* s = smem_base();
@@ -663,11 +690,23 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
                     uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
                     tma_load_2d(a, tmA, kb * BK, inf.row0, fb);
+                    if (p.gated) {
+                        // 128 columns of W1 into the first half of the B stage, of W3 into the second
 #pragma unroll
-                    for (int q = 0; q < BN / 64; ++q) {
-                        const int col = inf.nbk * BN + q * 64;
-                        // chunks past F read as zeros (out of bounds fill)
-                        tma_load_2d(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK, fb);
+                        for (int q = 0; q < GATED_BN / 64; ++q) {
+                            const int col = inf.nbk * GATED_BN + q * 64;
+                            const int c = col < ncol ? col : ncol;
+                            tma_load_2d(b + q * B_CHUNK_BYTES, tmB, c, inf.e * p.H + kb * BK, fb);
+                            tma_load_2d(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, c, inf.e * p.H + kb * BK, fb);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < BN / 64; ++q) {
+                            const int col = inf.nbk * BN + q * 64;
+                            // chunks past F read as zeros (out of bounds fill)
+                            tma_load_2d(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK,
+                                        fb);
+                        }
                     }
                     issued_any |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -714,8 +753,17 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                         const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
                         // B: N-major, 128B swizzle; 64-column chunks 8 KiB apart (LBO),
                         // 8-row K groups 1024 B apart (SBO); +2 KiB per K=16
-                        const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
-                        tc_mma_f16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        if (p.gated) {
+                            // gate and up projections side by side in the accumulator:
+                            // columns [0, 128) = A.W1, [128, 256) = A.W3
+                            const uint64_t b1 = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
+                            const uint64_t b3 = umma_desc_sw128(b0 + B_STAGE_BYTES / 2 + kk * 2048, B_CHUNK_BYTES, 1024);
+                            tc_mma_f16(d, ad, b1, IDESC_GATED, (kb | kk) != 0 ? 1u : 0u);
+                            tc_mma_f16(d + GATED_BN, ad, b3, IDESC_GATED, (kb | kk) != 0 ? 1u : 0u);
+                        } else {
+                            const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
+                            tc_mma_f16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     issued = true;
                     tc_commit(&cs->empty[stage]);
@@ -753,35 +801,35 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             const int rloc = quad * 32 + lane;
             const bool rowok = rloc < inf.nrows;
             const size_t row = size_t(inf.row0) + rloc;
-            const int n0 = inf.nbk * BN;
             const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + acc * BN;
+            if (p.gated) {
+                const int n0 = inf.nbk * GATED_BN;
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                const int col = n0 + cc * 32;
-                if (col >= p.F) break;
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + cc * 32, r);
-                tmem_ld_wait();
-                if (rowok) {
-                    if (p.out_f32) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.y) + row * p.F + col);
+                for (int cc = 0; cc < GATED_BN / 32; ++cc) {
+                    const int col = n0 + cc * 32;
+                    if (col >= p.F) break;
+                    uint32_t r[32], r3[32];
+                    tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                    tmem_ld_32x32b_x32(tbase + GATED_BN + cc * 32, r3);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + row * p.F + col);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * u]),
-                                                                               __uint_as_float(r[8 * v + 2 * u + 1]));
-                                pk[u] = *reinterpret_cast<const uint32_t*>(&h);
-                            }
-                            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
+                    for (int i = 0; i < 32; ++i) {
+                        // SwiGLU: silu(a) * b, silu(a) = a / (1 + e^-a)
+                        const float a = __uint_as_float(r[i]);
+                        r[i] = __float_as_uint(a / (1.f + expf(-a)) * __uint_as_float(r3[i]));
                     }
+                    if (rowok) store_row32(p, row, col, r);
+                }
+            } else {
+                const int n0 = inf.nbk * BN;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    const int col = n0 + cc * 32;
+                    if (col >= p.F) break;
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                    tmem_ld_wait();
+                    if (rowok) store_row32(p, row, col, r);
                 }
             }
             tc_fence_before();
@@ -1166,7 +1214,8 @@ __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
 
 template <int PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    mk_fused_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    mk_fused_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB3) {
     CtrlSmem* cs = ctrl();
     const uint32_t flag = 1u;  // tile ready / call aborted
     const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
@@ -1230,7 +1279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (cs->bcast[2]) {
             stamp(p, 6);
             if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, true, flag, w);
-            else compute_role(p, &tmA, &tmB, cs, true, flag, w);
+            else compute_role(p, &tmA, &tmB, &tmB3, cs, true, flag, w);
             stamp(p, 7);
         }
     }
@@ -1299,7 +1348,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_combine_kernel(const Params p)
 // Unfused baseline, launch 4: persistent expert GEMM over all tiles.
 template <int PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    mk_gemm_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    mk_gemm_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB3) {
     CtrlSmem* cs = ctrl();
     const uint32_t flag = 1u;
     const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
@@ -1313,7 +1363,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     build_tables(p, cs);
     __syncthreads();
     if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, false, flag, w);
-    else compute_role(p, &tmA, &tmB, cs, false, flag, w);
+    else compute_role(p, &tmA, &tmB, &tmB3, cs, false, flag, w);
     cta_teardown<PAIR>(p, cs, true);
 }
 
@@ -1324,7 +1374,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // clusters of two; if the driver refuses the cooperative attribute together
 // with clusters, it is launched without it after an occupancy check that
 // every cluster fits at once.
-cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st) {
+cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, int grid,
+                         cudaStream_t st) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NTHREADS);
@@ -1336,14 +1387,14 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
     cfg.attrs = attr;
     if (!p.pair) {
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, mk_fused_kernel<0>, p, a, b);
+        return cudaLaunchKernelEx(&cfg, mk_fused_kernel<0>, p, a, b, b3);
     }
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 2;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3);
     if (err == cudaSuccess) return err;
     (void)cudaGetLastError();
     cfg.attrs = attr + 1;
@@ -1351,10 +1402,11 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
     int clusters = 0;
     if ((err = cudaOccupancyMaxActiveClusters(&clusters, mk_fused_kernel<1>, &cfg)) != cudaSuccess) return err;
     if (2 * clusters < grid) return cudaErrorCooperativeLaunchTooLarge;
-    return cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b);
+    return cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3);
 }
 
-cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t st) {
+cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                           int grid, cudaStream_t st) {
     mk_route_kernel<<<p.nch, NTHREADS, SMEM_BYTES, st>>>(p);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
@@ -1363,7 +1415,7 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     mk_gather_kernel<<<p.nch, NTHREADS, SMEM_BYTES, st>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (!p.pair) {
-        mk_gemm_kernel<0><<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b);
+        mk_gemm_kernel<0><<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b, b3);
         if ((err = cudaGetLastError()) != cudaSuccess || !p.combine_out) return err;
         mk_combine_kernel<<<grid, NTHREADS, 0, st>>>(p);
         return cudaGetLastError();
@@ -1380,7 +1432,7 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((err = cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b)) != cudaSuccess || !p.combine_out) return err;
+    if ((err = cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b, b3)) != cudaSuccess || !p.combine_out) return err;
     mk_combine_kernel<<<grid, NTHREADS, 0, st>>>(p);
     return cudaGetLastError();
 }

@@ -844,72 +844,88 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
 
 // out[t,:] = sum_j gate[t,j] * y_sorted[row_of(t,j), :], fp32 in slot order
 // (deterministic, no atomics), stored in y_sorted's dtype.  Tokens are
-// spread over CTAs [first, first + stride, ...); each thread owns 16-byte
-// column chunks, two in flight.
-__device__ void combine_tokens(const Params& p, int first, int stride) {
-    const int k = p.k, F = p.F;
-    const int nchunk = F / 8;  // 8 values per chunk (16 B of bf16, 32 B of f32)
+// spread over CTAs [first, first + stride, ...).  The pass is HBM-bound, so
+// each thread first issues 16 independent 16-byte loads (16/K column
+// vectors of the token's K rows) and only then accumulates and stores.
+template <int K>
+__device__ void combine_tokens_k(const Params& p, int first, int stride) {
+    constexpr int U = 16 / K;  // 16-byte vectors per thread per pass
+    const int F = p.F;
+    const bool f32 = p.out_f32 != 0;
+    const int nvec = f32 ? F / 4 : F / 8;
     for (int t = first; t < p.T; t += stride) {
-        int r[MAX_K];
-        float g[MAX_K];
+        const uint4* src[K];
+        float g[K];
 #pragma unroll
-        for (int j = 0; j < MAX_K; ++j) {
+        for (int j = 0; j < K; ++j) {
             // in range even if an error path left a row unrecorded
-            r[j] = j < k ? min(max(__ldcg(p.row_of + size_t(t) * k + j), 0), p.rows - 1) : 0;
-            g[j] = j < k ? __ldcg(p.topk_gate + size_t(t) * k + j) : 0.f;
+            const int r = min(max(__ldcg(p.row_of + size_t(t) * K + j), 0), p.rows - 1);
+            src[j] = f32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(p.y) + size_t(r) * F)
+                         : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.y) + size_t(r) * F);
+            g[j] = __ldcg(p.topk_gate + size_t(t) * K + j);
         }
-        for (int c0 = threadIdx.x; c0 < nchunk; c0 += 2 * NTHREADS) {
-            float acc[2][8];
+        uint4* dst = f32 ? reinterpret_cast<uint4*>(static_cast<float*>(p.combine_out) + size_t(t) * F)
+                         : reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.combine_out) + size_t(t) * F);
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += U * NTHREADS) {
+            uint4 buf[U][K];
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * NTHREADS;
 #pragma unroll
-                for (int v = 0; v < 8; ++v) acc[u][v] = 0.f;
+                for (int j = 0; j < K; ++j) buf[u][j] = v < nvec ? __ldcg(src[j] + v) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-            for (int j = 0; j < MAX_K; ++j) {
-                if (j >= k) break;
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * NTHREADS;
+                if (v >= nvec) break;
+                if (f32) {
+                    float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int c = c0 + u * NTHREADS;
-                    if (c >= nchunk) continue;
-                    if (p.out_f32) {
-                        const float4* src = reinterpret_cast<const float4*>(
-                            static_cast<const float*>(p.y) + size_t(r[j]) * F + size_t(c) * 8);
-                        const float4 a = __ldcg(src), b = __ldcg(src + 1);
-                        acc[u][0] += g[j] * a.x; acc[u][1] += g[j] * a.y; acc[u][2] += g[j] * a.z; acc[u][3] += g[j] * a.w;
-                        acc[u][4] += g[j] * b.x; acc[u][5] += g[j] * b.y; acc[u][6] += g[j] * b.z; acc[u][7] += g[j] * b.w;
-                    } else {
-                        const uint4 q = __ldcg(reinterpret_cast<const uint4*>(
-                            static_cast<const uint16_t*>(p.y) + size_t(r[j]) * F + size_t(c) * 8));
-                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                    for (int j = 0; j < K; ++j) {
+                        a[0] += g[j] * __uint_as_float(buf[u][j].x);
+                        a[1] += g[j] * __uint_as_float(buf[u][j].y);
+                        a[2] += g[j] * __uint_as_float(buf[u][j].z);
+                        a[3] += g[j] * __uint_as_float(buf[u][j].w);
+                    }
+                    dst[v] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                        __float_as_uint(a[3]));
+                } else {
+                    float a[8];
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[v]));
-                            acc[u][2 * v] += g[j] * f.x;
-                            acc[u][2 * v + 1] += g[j] * f.y;
+                    for (int i = 0; i < 8; ++i) a[i] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < K; ++j) {
+                        const uint32_t w4[4] = {buf[u][j].x, buf[u][j].y, buf[u][j].z, buf[u][j].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
+                            a[2 * q] += g[j] * f.x;
+                            a[2 * q + 1] += g[j] * f.y;
                         }
                     }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int c = c0 + u * NTHREADS;
-                if (c >= nchunk) continue;
-                if (p.out_f32) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.combine_out) + size_t(t) * F + size_t(c) * 8);
-                    dst[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
-                    dst[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
-                } else {
                     uint32_t pk[4];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[u][2 * v], acc[u][2 * v + 1]);
-                        pk[v] = *reinterpret_cast<const uint32_t*>(&h);
+                    for (int q = 0; q < 4; ++q) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * q], a[2 * q + 1]);
+                        pk[q] = *reinterpret_cast<const uint32_t*>(&h);
                     }
-                    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.combine_out) + size_t(t) * F + size_t(c) * 8) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
         }
+    }
+}
+
+__device__ void combine_tokens(const Params& p, int first, int stride) {
+    switch (p.k) {
+        case 1: combine_tokens_k<1>(p, first, stride); break;
+        case 2: combine_tokens_k<2>(p, first, stride); break;
+        case 3: combine_tokens_k<3>(p, first, stride); break;
+        case 4: combine_tokens_k<4>(p, first, stride); break;
+        case 5: combine_tokens_k<5>(p, first, stride); break;
+        case 6: combine_tokens_k<6>(p, first, stride); break;
+        case 7: combine_tokens_k<7>(p, first, stride); break;
+        default: combine_tokens_k<8>(p, first, stride); break;
     }
 }
 

@@ -91,8 +91,18 @@ typedef struct mk_config {
                                <= 0 = off (the default)                          */
     int32_t mma_pair;       /* MK_MMA_*: one SM per 128-row tile, or an SM pair
                                (cta_group::2) per 256-row tile                  */
-    int32_t reserved[5];    /* must be zero                                     */
+    int32_t gather;         /* MK_GATHER_*: where the GEMM's token rows come from */
+    int32_t reserved[4];    /* must be zero                                     */
 } mk_config_t;
+
+/* Token rows for the GEMM.  STAGED: dispatch CTAs copy them into
+ * expert-contiguous tiles in the workspace and release a flag per tile;
+ * compute CTAs wait on the flag and load whole tiles.  DIRECT: the GEMM's
+ * producer warp copies each tile's rows straight from x into its
+ * shared-memory stages (16-byte cp.async), so there is no staging copy, no
+ * gather role, and the workspace holds no staging rows (T*k*H*2 bytes
+ * less); single-SM tiles only, and T*H*2 < 4 GiB.  AUTO = STAGED. */
+enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
 
 /* Expert GEMM tile.  SINGLE: each CTA runs a 128 x 256 tile alone.  PAIR: a
  * cluster of two CTAs (two SMs) runs a 256 x 256 tile with the 2-SM tensor
@@ -108,7 +118,7 @@ typedef struct mk_launch_info {
     int32_t n_group;
     int64_t workspace_bytes;
     int32_t mma_pair;       /* MK_MMA_SINGLE or MK_MMA_PAIR as resolved */
-    int32_t reserved0;
+    int32_t gather;         /* MK_GATHER_STAGED or MK_GATHER_DIRECT as resolved */
 } mk_launch_info_t;
 
 /* Fill `cfg` with the defaults (fused, bf16 output, heuristic split). */

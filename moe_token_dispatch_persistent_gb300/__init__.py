@@ -34,6 +34,9 @@ MK_FAULT_DROP_TILE_FLAG = 1
 MK_MMA_AUTO = 0
 MK_MMA_SINGLE = 1
 MK_MMA_PAIR = 2
+MK_GATHER_AUTO = 0
+MK_GATHER_STAGED = 1
+MK_GATHER_DIRECT = 2
 
 # Entry points declared in include/mk.h (checked by the tests).
 ABI_FUNCTIONS = (
@@ -77,7 +80,8 @@ class mk_config_t(ctypes.Structure):
         ("trace", ctypes.c_int32),
         ("l2_prefetch", ctypes.c_int32),
         ("mma_pair", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("gather", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
 
@@ -89,7 +93,7 @@ class mk_launch_info_t(ctypes.Structure):
         ("n_group", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
         ("mma_pair", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("gather", ctypes.c_int32),
     ]
 
 
@@ -309,11 +313,11 @@ def mk_release_workspace() -> None:
 
 def make_config(mode=MK_MODE_FUSED, out_dtype=MK_OUT_BF16, dispatch_ctas=0, grid_ctas=0, n_group=0,
                 debug_fault=MK_FAULT_NONE, spin_limit_ns=0, trace=0, l2_prefetch=0,
-                mma_pair=0) -> mk_config_t:
+                mma_pair=0, gather=0) -> mk_config_t:
     c = mk_config_default()
     c.mode, c.out_dtype, c.dispatch_ctas, c.grid_ctas = mode, out_dtype, dispatch_ctas, grid_ctas
     c.n_group, c.debug_fault, c.spin_limit_ns, c.trace = n_group, debug_fault, spin_limit_ns, trace
-    c.l2_prefetch, c.mma_pair = l2_prefetch, mma_pair
+    c.l2_prefetch, c.mma_pair, c.gather = l2_prefetch, mma_pair, gather
     return c
 
 

@@ -144,6 +144,17 @@ int dispatch_split(int grid, int T, int H, int F, int k) {
 
 // Tile height: SM pairs (256-row tiles, 2-SM MMA) unless asked otherwise.
 // AUTO keeps single-SM tiles until the pair path is measured on a shape.
+// Where the GEMM's token rows come from.  STAGED: the dispatch role copies
+// them into expert-contiguous tiles and flags each tile.  DIRECT: the GEMM's
+// producer warp copies them from x itself (no staging rows in the
+// workspace, no gather role).  Dispatch-only always stages (it measures the
+// gather); AUTO stages (measured on GB300: direct is at par on the skewed
+// and imbalanced workloads and slower on the Mixtral-like one).
+int resolve_gather(const mk_config_t& c) {
+    if (c.mode == MK_MODE_DISPATCH_ONLY) return MK_GATHER_STAGED;
+    return c.gather == MK_GATHER_DIRECT ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
+}
+
 int resolve_pair(const mk_config_t& c, int T, int E, int k) {
     (void)T;
     (void)E;
@@ -225,7 +236,8 @@ const char* mk_status_string(mk_status_t s) {
 size_t mk_workspace_size(int T, int H, int F, int E, int k, const mk_config_t* cfg) {
     (void)cfg;
     if (validate_sizes(T, H, E, k, F) != MK_OK) return 0;
-    return ws_layout(T, H, E, k).total;
+    const mk_config_t c = config_or_default(cfg);
+    return ws_layout(T, H, E, k, resolve_gather(c) == MK_GATHER_STAGED).total;
 }
 
 }  // extern "C"
@@ -241,9 +253,10 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     mk_status_t s = validate_sizes(T, H, E, k, F);
     if (s != MK_OK) return s;
     const mk_config_t c = config_or_default(cfg_in);
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 4; ++i)
         if (c.reserved[i] != 0) return MK_ERR_INVALID_ARG;
     if (c.mma_pair < MK_MMA_AUTO || c.mma_pair > MK_MMA_PAIR) return MK_ERR_INVALID_ARG;
+    if (c.gather < MK_GATHER_AUTO || c.gather > MK_GATHER_DIRECT) return MK_ERR_INVALID_ARG;
     if (c.mode < MK_MODE_FUSED || c.mode > MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
     if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
     if (c.debug_fault != MK_FAULT_NONE && c.debug_fault != MK_FAULT_DROP_TILE_FLAG) return MK_ERR_INVALID_ARG;
@@ -271,13 +284,17 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
 
     const bool pair = resolve_pair(c, T, E, k) == MK_MMA_PAIR;
     if (pair && W3) return MK_ERR_UNSUPPORTED;  // the gated FFN runs on single-SM tiles
+    const bool direct = resolve_gather(c) == MK_GATHER_DIRECT;
+    if (direct && pair) return MK_ERR_UNSUPPORTED;  // SM pairs load staged rows only
+    // direct rows are addressed with 32-bit byte offsets into x
+    if (direct && uint64_t(T) * uint64_t(H) * 2 >= (uint64_t(1) << 32)) return MK_ERR_UNSUPPORTED;
     int grid = grid_for(*d, c);
     if (pair) grid &= ~1;  // whole clusters of two
     if (grid < (pair ? 2 : 1)) return MK_ERR_UNSUPPORTED;
     const int rows = T * k;
     const int nch = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
     if (nch > grid * MAX_CHUNKS_PER_CTA) return MK_ERR_UNSUPPORTED;
-    const WsLayout L = ws_layout(T, H, E, k);
+    const WsLayout L = ws_layout(T, H, E, k, !direct);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (ws) {
         if (ws_bytes < L.total || !aligned(ws, 256)) return MK_ERR_WORKSPACE;
@@ -311,8 +328,11 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.n_group = c.n_group > 0 ? (c.n_group < p.nb ? c.n_group : p.nb) : n_group_for(H, F, p.nb);
     p.mode = c.mode;
     p.compute = c.mode != MK_MODE_DISPATCH_ONLY;
+    p.direct = direct ? 1 : 0;
     if (c.mode == MK_MODE_DISPATCH_ONLY) {
         p.dispatch_ctas = grid;
+    } else if (direct) {
+        p.dispatch_ctas = 0;  // rows go straight into the GEMM's shared memory: no gather role
     } else {
         p.dispatch_ctas = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
         if (p.dispatch_ctas > grid) p.dispatch_ctas = grid;
@@ -347,7 +367,9 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
-    if (encode_2d(&tmA, p.xs, uint64_t(H), uint64_t(rows), uint64_t(H) * 2, BK, BM) != CUDA_SUCCESS)
+    // A: the staging rows (staged); encoded over x when there are none (unused then)
+    if (encode_2d(&tmA, direct ? x : static_cast<const void*>(p.xs), uint64_t(H), uint64_t(direct ? T : rows),
+                  uint64_t(H) * 2, BK, BM) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
     if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
@@ -370,6 +392,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     g_last_info.dispatch_ctas = c.mode == MK_MODE_UNFUSED ? 0 : p.dispatch_ctas;
     g_last_info.n_group = p.n_group;
     g_last_info.mma_pair = pair ? MK_MMA_PAIR : MK_MMA_SINGLE;
+    g_last_info.gather = direct ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
     g_last_info.workspace_bytes = int64_t(L.total);
     if (getenv("MK_LOG"))
         fprintf(stderr, "[mk] T=%d H=%d F=%d E=%d k=%d mode=%d grid=%d dispatch=%d n_group=%d slots=%d ws=%zu\n", T, H,

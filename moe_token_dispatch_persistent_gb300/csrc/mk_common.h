@@ -124,6 +124,7 @@ struct Params {
     int l2_prefetch;         // W k-blocks prefetched into L2 ahead of the TMA loads (0: off)
     int pair;                // 1: 2-SM MMA (cluster of 2 CTAs per 256-row tile)
     int gated;               // 1: y = silu(x.W1) * (x.W3), 128-column N-blocks
+    int direct;              // 1: the GEMM's producer copies token rows from x (no staging rows)
     int tile_rows;           // rows per tile: 128, or 256 with pair
     int trace;
     long long spin_limit_ns;
@@ -151,7 +152,7 @@ inline size_t ws_align(size_t v) { return (v + 255) & ~size_t(255); }
 
 constexpr int MAX_GRID = 1024;
 
-inline WsLayout ws_layout(int T, int H, int E, int k, int grid = MAX_GRID) {
+inline WsLayout ws_layout(int T, int H, int E, int k, bool staging = true, int grid = MAX_GRID) {
     WsLayout L{};
     const size_t rows = size_t(T) * k;
     const size_t nch = (size_t(T) + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
@@ -166,7 +167,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, int grid = MAX_GRID) {
     L.bases = o;      o = ws_align(o + nch * E * 4);
     L.ready = o;      o = ws_align(o + max_tiles * 4);
     L.trace = o;      o = ws_align(o + size_t(grid) * TRACE_SLOTS * 8);
-    L.xs = o;         o = ws_align(o + rows * size_t(H) * 2);
+    L.xs = o;         o = ws_align(o + (staging ? rows * size_t(H) * 2 : 0));
     L.total = o;
     return L;
 }

@@ -428,7 +428,7 @@ __device__ void scatter_chunk(const Params& p, int c, const int* cbase, const Wa
             const int i = i0 + u * NTHREADS;
             if (i >= n) continue;
             const int q = t0 * k + i;
-            const int dest = cbase[min(max(e[u], 0), MAX_E - 1)] + lr[u];
+            const int dest = cbase[min(max(e[u], 0), p.E - 1)] + lr[u];
             if (dest < 0 || dest >= p.rows) {
                 record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(dest));
                 raise_abort(w);
@@ -612,6 +612,125 @@ __device__ __forceinline__ void store_row32(const Params& p, size_t row, int col
     }
 }
 
+// Direct-gather producer (all 32 lanes of warp 0; no staging rows, no tile
+// flags).  Per item lane 0 takes a work item from the queue and publishes it;
+// per K-block lane 0 arms the stage with the TMA bytes of B (W boxes, as in
+// the staged path) while all lanes copy the tile's 128 token rows straight
+// from x with 16-byte cp.async into the 128-byte-swizzled layout the MMA
+// reads: lane (c = lane % 8, rq = lane / 8) copies chunk c of rows 4i + rq,
+// so each warp instruction reads four whole 128-byte lines, and chunk c of
+// row r lands at r*128 + ((c ^ (r % 8)) * 16).  Each lane then arms an
+// asynchronous arrival on the stage's full barrier that fires once its
+// copies have landed (33 arrivals per phase); the MMA thread orders those
+// generic-proxy writes before the tensor core's reads with a proxy fence.
+__device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const CUtensorMap* tmB3, CtrlSmem* cs,
+                                const WaitCtx& wp) {
+    const int lane = threadIdx.x & 31;
+    uint8_t* s = smem_base();
+    const int total_items = cs->item_start[p.E];
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_par = 0, issued_any = 0;
+    bool ok = true;
+    uint32_t next = 0;
+    if (lane == 0) next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+    for (uint32_t it = 0;; ++it) {
+        const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+        int go = 1;  // 1: an item to run, 0: queue empty, -1: gave up
+        Info inf{0, 0, 0, 0};
+        if (lane == 0) {
+            const int item = int(next);
+            int gtile = 0;
+            if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+                go = -1;
+            } else if (item >= total_items) {
+                cs->info[slot].e = -1;
+                mbar_arrive(&cs->info_full[slot]);
+                go = 0;
+            } else {
+                next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+                decode_item(p, cs, item, inf, gtile);
+                cs->info[slot] = inf;
+                mbar_arrive(&cs->info_full[slot]);
+            }
+        }
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (go <= 0) {
+            ok = go == 0;
+            break;
+        }
+        inf.e = __shfl_sync(0xffffffffu, inf.e, 0);
+        inf.row0 = __shfl_sync(0xffffffffu, inf.row0, 0);
+        inf.nrows = __shfl_sync(0xffffffffu, inf.nrows, 0);
+        inf.nbk = __shfl_sync(0xffffffffu, inf.nbk, 0);
+        // byte offset in x of the 32 tile rows this lane copies (rows past the
+        // tile repeat its first row; their products are never stored)
+        uint32_t rowoff[BM / 4];
+#pragma unroll
+        for (int i = 0; i < BM / 4; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const int q = __ldcg(p.src_index + inf.row0 + (r < inf.nrows ? r : 0));
+            rowoff[i] = uint32_t(min(max(q / p.k, 0), p.T - 1)) * uint32_t(p.H) * 2u;
+        }
+        const int ncol = p.F;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            int okk = 1;
+            if (lane == 0) {
+                if (!wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) okk = 0;
+                else mbar_arrive_expect_tx(&cs->full[stage], B_STAGE_BYTES);
+            }
+            okk = __shfl_sync(0xffffffffu, okk, 0);  // also orders lane 0's expect-tx first
+            if (!okk) {
+                ok = false;
+                break;
+            }
+            uint64_t* fb = &cs->full[stage];
+            uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
+            uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
+            {
+                const int c = lane & 7, rq = lane >> 3;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(p.x) + kb * (BK * 2) + c * 16;
+                const uint32_t d0 = smem_u32(a) + rq * 128 + ((c ^ rq) << 4);             // rows 4i + rq, i even
+                const uint32_t d1 = smem_u32(a) + (4 + rq) * 128 + ((c ^ (4 + rq)) << 4);  // i odd: row % 8 = 4 + rq
+#pragma unroll
+                for (int i = 0; i < BM / 4; ++i)
+                    cp_async_16_u32(((i & 1) ? d1 - 512 : d0) + 512 * i, src + rowoff[i]);
+                cp_async_mbar_arrive_noinc(fb);
+            }
+            if (lane == 0) {
+                if (p.gated) {
+#pragma unroll
+                    for (int q = 0; q < GATED_BN / 64; ++q) {
+                        const int col = inf.nbk * GATED_BN + q * 64;
+                        const int cc = col < ncol ? col : ncol;
+                        tma_load_2d(b + q * B_CHUNK_BYTES, tmB, cc, inf.e * p.H + kb * BK, fb);
+                        tma_load_2d(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, cc, inf.e * p.H + kb * BK, fb);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < BN / 64; ++q) {
+                        const int col = inf.nbk * BN + q * 64;
+                        tma_load_2d(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK, fb);
+                    }
+                }
+                issued_any |= 1u << stage;
+                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+    }
+    cp_async_wait_all();  // no copy of this warp outlives the role
+    if (!ok && lane == 0) {
+        WaitCtx shortw{nullptr, 0u, 5000000LL};
+        for (int st = 0; st < STAGES; ++st)
+            if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
+    }
+    __syncwarp();
+}
+
 // Warp-specialised expert GEMM over work items (tile, N-block) taken from the
 // shared queue until it is empty.  wait_ready: spin on the tile's flag first.
 __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmB3,
@@ -625,7 +744,9 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     // that times out and is recorded is the one at the root.
     const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
 
-    if (warp == 0) {
+    if (warp == 0 && p.direct) {
+        producer_direct(p, tmB, tmB3, cs, wp);
+    } else if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
             uint32_t stage = 0, phase = 0;
@@ -744,6 +865,9 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                         ok = false;
                         break;
                     }
+                    // direct rows were written by cp.async (generic proxy): order
+                    // them before the tensor core reads the stage
+                    if (p.direct) fence_proxy_async_shared();
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(s + SM_A + stage * A_STAGE_BYTES);
                     const uint32_t b0 = smem_u32(s + SM_B + stage * B_STAGE_BYTES);
@@ -1161,11 +1285,11 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
 // leader's MMA thread and 4 epilogue warps plus the peer's producer and 4
 // epilogue warps (10); those two live in the leader only.
 template <int PAIR>
-__device__ void cta_setup(CtrlSmem* cs, bool with_tmem) {
+__device__ void cta_setup(CtrlSmem* cs, bool with_tmem, bool direct) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int i = 0; i < MAX_STAGES; ++i) {
-            mbar_init(&cs->full[i], 1);
+            mbar_init(&cs->full[i], direct ? 1 + 32 : 1);  // direct: + one cp.async arrival per producer lane
             mbar_init(&cs->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1241,7 +1365,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    cta_setup<PAIR>(cs, p.compute != 0);
+    cta_setup<PAIR>(cs, p.compute != 0, p.direct != 0);
 
     // This call's readiness flags start at 0.  Cleared before the routing
     // barrier; they are set only after it, so no stale value is ever seen.
@@ -1289,13 +1413,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncthreads();
             stamp(p, 5);
         }
-        if (threadIdx.x == 0) cs->bcast[2] = p.compute && !aborted(w);
+        if (threadIdx.x == 0) {
+            bool go = p.compute && !aborted(w);
+            // direct rows: the producers read src_index rows that every CTA scattered
+            if (go && p.direct) go = wait_geq(&p.ctl->bar_scattered, gridDim.x, w, SITE_BAR_SCATTERED);
+            cs->bcast[2] = go;
+        }
         fence_proxy_async_shared();  // generic/bulk smem use before TMA writes into it
         __syncthreads();
         if (cs->bcast[2]) {
             stamp(p, 6);
             if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, true, flag, w);
-            else compute_role(p, &tmA, &tmB, &tmB3, cs, true, flag, w);
+            else compute_role(p, &tmA, &tmB, &tmB3, cs, !p.direct, flag, w);
             stamp(p, 7);
         }
     }
@@ -1352,6 +1481,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_gather_kernel(const Params p) 
     }
     __syncthreads();
     const WaitCtx w{nullptr, 0u, p.spin_limit_ns};
+    if (p.direct) {
+        // rows are copied by the GEMM itself: only src_index / gate_w / row_of here
+        scatter_chunk(p, blockIdx.x, p.bases + size_t(blockIdx.x) * p.E, w);
+        return;
+    }
     uint32_t ph = 0;
     push_gather_chunk(p, blockIdx.x, cs, ph, w);
 }
@@ -1373,7 +1507,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    cta_setup<PAIR>(cs, true);
+    cta_setup<PAIR>(cs, true, p.direct != 0);
     for (int e = threadIdx.x; e < p.E; e += NTHREADS) cs->tot[e] = p.expert_offsets[e + 1] - p.expert_offsets[e];
     __syncthreads();
     build_tables(p, cs);

@@ -49,8 +49,8 @@ def test_status_strings(lib):
 def test_config_defaults(lib):
     c = mk.mk_config_default()
     assert c.mode == mk.MK_MODE_FUSED and c.out_dtype == mk.MK_OUT_BF16
-    assert c.dispatch_ctas == 0 and c.spin_limit_ns == 0 and list(c.reserved) == [0] * 5 and c.l2_prefetch == 0
-    assert c.mma_pair == mk.MK_MMA_AUTO
+    assert c.dispatch_ctas == 0 and c.spin_limit_ns == 0 and list(c.reserved) == [0] * 4 and c.l2_prefetch == 0
+    assert c.mma_pair == mk.MK_MMA_AUTO and c.gather == mk.MK_GATHER_AUTO
 
 
 def test_struct_layouts_match_header(lib):

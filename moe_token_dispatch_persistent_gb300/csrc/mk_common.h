@@ -19,7 +19,13 @@ constexpr int B_CHUNK_BYTES = BK * 64 * 2;            //  8 KiB: 64 rows of K x 
 constexpr int B_STAGE_BYTES = BK * BN * 2;            // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                     // two fp32 accumulators
-constexpr int NWARPS = 6;                             // producer, MMA, 4 x epilogue
+constexpr int EPI_WARP_END = 6;                       // warps 2..5: epilogue (TMEM lane quads 2, 3, 0, 1)
+// Direct gather: warp 0 and warps 6.. copy the A rows.  Two beat one by 4-12%
+// on GB300; four do not help (nine warps cap registers at 168 and spill).
+constexpr int COPY_WARPS = 2;
+constexpr int NWARPS = EPI_WARP_END + COPY_WARPS - 1; // producer, MMA, 4 x epilogue, copy helpers
+constexpr int COPY_ROWS = BM / COPY_WARPS;            // A rows per copy warp and stage
+static_assert(COPY_ROWS % 8 == 0, "each copy warp owns whole 8-row swizzle atoms");
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int ROUTE_CHUNK = NWARPS * 32;              // tokens per routing chunk (lane per token)
 constexpr int MAX_E = 256;

@@ -612,45 +612,58 @@ __device__ __forceinline__ void store_row32(const Params& p, size_t row, int col
     }
 }
 
-// Direct-gather producer (all 32 lanes of warp 0; no staging rows, no tile
-// flags).  Per item lane 0 takes a work item from the queue and publishes it;
-// per K-block lane 0 arms the stage with the TMA bytes of B (W boxes, as in
-// the staged path) while all lanes copy the tile's 128 token rows straight
-// from x with 16-byte cp.async into the 128-byte-swizzled layout the MMA
-// reads: lane (c = lane % 8, rq = lane / 8) copies chunk c of rows 4i + rq,
-// so each warp instruction reads four whole 128-byte lines, and chunk c of
-// row r lands at r*128 + ((c ^ (r % 8)) * 16).  Each lane then arms an
-// asynchronous arrival on the stage's full barrier that fires once its
-// copies have landed (33 arrivals per phase); the MMA thread orders those
+// Direct-gather producer: COPY_WARPS warps (warp 0, the leader, and warps
+// 6..), no staging rows, no tile flags.  Per item the leader's lane 0 takes a
+// work item from the queue and publishes it; the helpers read it from the
+// same info slot.  Per K-block the leader arms the stage with the TMA bytes
+// of B (W boxes, as in the staged path), and every copy warp copies its
+// COPY_ROWS token rows of the tile straight from x with 16-byte cp.async
+// into the 128-byte-swizzled layout the MMA reads: lane (c = lane % 8,
+// rq = lane / 8) copies chunk c of rows 4i + rq of the warp's slice, so each
+// warp instruction reads four whole 128-byte lines, and chunk c of row r
+// lands at r*128 + ((c ^ (r % 8)) * 16).  Each lane then arms an asynchronous
+// arrival on the stage's full barrier that fires once its copies have landed
+// (1 + 32 * COPY_WARPS arrivals per phase); the MMA thread orders those
 // generic-proxy writes before the tensor core's reads with a proxy fence.
+// One warp alone cannot issue the copies as fast as the tensor core consumes
+// them, hence several.
 __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const CUtensorMap* tmB3, CtrlSmem* cs,
-                                const WaitCtx& wp) {
+                                const int cw, const WaitCtx& wp) {
     const int lane = threadIdx.x & 31;
+    const bool leader = cw == 0;
     uint8_t* s = smem_base();
     const int total_items = cs->item_start[p.E];
     uint32_t stage = 0, phase = 0;
     uint32_t issued_par = 0, issued_any = 0;
     bool ok = true;
     uint32_t next = 0;
-    if (lane == 0) next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+    if (leader && lane == 0) next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
     for (uint32_t it = 0;; ++it) {
         const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
         int go = 1;  // 1: an item to run, 0: queue empty, -1: gave up
         Info inf{0, 0, 0, 0};
         if (lane == 0) {
-            const int item = int(next);
-            int gtile = 0;
-            if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+            if (leader) {
+                const int item = int(next);
+                int gtile = 0;
+                if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+                    go = -1;
+                } else if (item >= total_items) {
+                    cs->info[slot].e = -1;
+                    mbar_arrive(&cs->info_full[slot]);
+                    go = 0;
+                } else {
+                    next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+                    decode_item(p, cs, item, inf, gtile);
+                    cs->info[slot] = inf;
+                    mbar_arrive(&cs->info_full[slot]);
+                }
+            } else if (!wait_mbar(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) {
                 go = -1;
-            } else if (item >= total_items) {
-                cs->info[slot].e = -1;
-                mbar_arrive(&cs->info_full[slot]);
-                go = 0;
             } else {
-                next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
-                decode_item(p, cs, item, inf, gtile);
-                cs->info[slot] = inf;
-                mbar_arrive(&cs->info_full[slot]);
+                inf = cs->info[slot];
+                mbar_arrive(&cs->info_empty[slot]);
+                go = inf.e < 0 ? 0 : 1;
             }
         }
         go = __shfl_sync(0xffffffffu, go, 0);
@@ -658,25 +671,22 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
             ok = go == 0;
             break;
         }
-        inf.e = __shfl_sync(0xffffffffu, inf.e, 0);
         inf.row0 = __shfl_sync(0xffffffffu, inf.row0, 0);
         inf.nrows = __shfl_sync(0xffffffffu, inf.nrows, 0);
-        inf.nbk = __shfl_sync(0xffffffffu, inf.nbk, 0);
-        // byte offset in x of the 32 tile rows this lane copies (rows past the
+        // byte offset in x of the tile rows this lane copies (rows past the
         // tile repeat its first row; their products are never stored)
-        uint32_t rowoff[BM / 4];
+        uint32_t rowoff[COPY_ROWS / 4];
 #pragma unroll
-        for (int i = 0; i < BM / 4; ++i) {
-            const int r = 4 * i + (lane >> 3);
+        for (int i = 0; i < COPY_ROWS / 4; ++i) {
+            const int r = cw * COPY_ROWS + 4 * i + (lane >> 3);
             const int q = __ldcg(p.src_index + inf.row0 + (r < inf.nrows ? r : 0));
             rowoff[i] = uint32_t(min(max(q / p.k, 0), p.T - 1)) * uint32_t(p.H) * 2u;
         }
-        const int ncol = p.F;
         for (int kb = 0; kb < p.kblocks; ++kb) {
             int okk = 1;
             if (lane == 0) {
                 if (!wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) okk = 0;
-                else mbar_arrive_expect_tx(&cs->full[stage], B_STAGE_BYTES);
+                else if (leader) mbar_arrive_expect_tx(&cs->full[stage], B_STAGE_BYTES);
             }
             okk = __shfl_sync(0xffffffffu, okk, 0);  // also orders lane 0's expect-tx first
             if (!okk) {
@@ -684,19 +694,20 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
                 break;
             }
             uint64_t* fb = &cs->full[stage];
-            uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
-            uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
+            uint8_t* a = s + SM_A + stage * A_STAGE_BYTES + cw * COPY_ROWS * 128;
             {
                 const int c = lane & 7, rq = lane >> 3;
                 const uint8_t* src = reinterpret_cast<const uint8_t*>(p.x) + kb * (BK * 2) + c * 16;
                 const uint32_t d0 = smem_u32(a) + rq * 128 + ((c ^ rq) << 4);             // rows 4i + rq, i even
                 const uint32_t d1 = smem_u32(a) + (4 + rq) * 128 + ((c ^ (4 + rq)) << 4);  // i odd: row % 8 = 4 + rq
 #pragma unroll
-                for (int i = 0; i < BM / 4; ++i)
+                for (int i = 0; i < COPY_ROWS / 4; ++i)
                     cp_async_16_u32(((i & 1) ? d1 - 512 : d0) + 512 * i, src + rowoff[i]);
                 cp_async_mbar_arrive_noinc(fb);
             }
-            if (lane == 0) {
+            if (leader && lane == 0) {
+                uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
+                const int ncol = p.F;
                 if (p.gated) {
 #pragma unroll
                     for (int q = 0; q < GATED_BN / 64; ++q) {
@@ -723,7 +734,7 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
         if (!ok) break;
     }
     cp_async_wait_all();  // no copy of this warp outlives the role
-    if (!ok && lane == 0) {
+    if (!ok && leader && lane == 0) {
         WaitCtx shortw{nullptr, 0u, 5000000LL};
         for (int st = 0; st < STAGES; ++st)
             if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
@@ -744,8 +755,8 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     // that times out and is recorded is the one at the root.
     const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
 
-    if (warp == 0 && p.direct) {
-        producer_direct(p, tmB, tmB3, cs, wp);
+    if (p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
+        producer_direct(p, tmB, tmB3, cs, warp == 0 ? 0 : warp - EPI_WARP_END + 1, wp);
     } else if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
@@ -909,7 +920,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < EPI_WARP_END) {
         // ---------------- epilogue: warps 2..5 ----------------
         const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32)
         uint32_t acc = 0, accph = 0;
@@ -1221,7 +1232,7 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < EPI_WARP_END) {
         // ---------------- epilogue: warps 2..5 of both CTAs ----------------
         const int quad = warp & 3;
         const uint32_t info_empty_leader = mapa_shared(smem_u32(&cs->info_empty[0]), 0);
@@ -1280,7 +1291,9 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
 }
 
 // Barrier arrival counts.  Single CTA: the producer's expect-tx, one commit,
-// 128 epilogue threads, the MMA thread + 4 epilogue warps.  Pair: acc_empty
+// 128 epilogue threads, the MMA thread + 4 epilogue warps.  Direct gather
+// adds one cp.async arrival per copy lane to each full barrier and one
+// info_empty arrival per copy helper warp.  Pair: acc_empty
 // gets one arrival per epilogue warp of both CTAs (8) and info_empty the
 // leader's MMA thread and 4 epilogue warps plus the peer's producer and 4
 // epilogue warps (10); those two live in the leader only.
@@ -1289,7 +1302,7 @@ __device__ void cta_setup(CtrlSmem* cs, bool with_tmem, bool direct) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int i = 0; i < MAX_STAGES; ++i) {
-            mbar_init(&cs->full[i], direct ? 1 + 32 : 1);  // direct: + one cp.async arrival per producer lane
+            mbar_init(&cs->full[i], direct ? 1 + 32 * COPY_WARPS : 1);
             mbar_init(&cs->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1298,7 +1311,7 @@ __device__ void cta_setup(CtrlSmem* cs, bool with_tmem, bool direct) {
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&cs->info_full[i], 1);
-            mbar_init(&cs->info_empty[i], PAIR ? 10 : 1 + 4);
+            mbar_init(&cs->info_empty[i], PAIR ? 10 : 1 + 4 + (direct ? COPY_WARPS - 1 : 0));
         }
         mbar_init(&cs->drain, 1);
         for (int i = 0; i < MAX_GATHER_SLOTS; ++i) mbar_init(&cs->gbar[i], 1);

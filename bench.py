@@ -19,6 +19,7 @@ Prints ONE JSON line on rank 0.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -44,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=sorted(synth.WORKLOADS))
@@ -125,55 +126,69 @@ def whole_job_tflops(flop_per_rank: float, world: int, seconds_max: float) -> fl
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
+        """Start sampling; returns once the first sample is written (or after 5 s)."""
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu), "-lms", "200"], stdout=self.fh,
+                                          "-i", str(self.gpu), "-lms", str(self.PERIOD_MS)], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        deadline = time.time() + 5.0
+        while time.time() < deadline and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+            time.sleep(0.02)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self):
+        """Median SM clock and the throttle reasons of the samples taken between
+        mark_start and mark_end (all samples if none fell inside)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons, n = [], [], set(), 0
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
                 except ValueError:
                     continue
-                n += 1
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(nm)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": n}
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({nm for r in use for nm, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside), "period_ms": self.PERIOD_MS}
 
 
 # ------------------------------------------------------------ reference --
@@ -347,8 +362,10 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     sampler.start()
     launches_before = 0
+    sampler.mark_start()
     ms = timed(cfg, args.steps, 0)
     torch.cuda.synchronize()
+    sampler.mark_end()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
@@ -426,6 +443,14 @@ def run_ours(args, w):
         line["gated"] = {"ms": gms, "tflops": 2 * w.flop / (gms / 1e3) / 1e12,
                          "frac_bf16": 2 * w.flop / (gms / 1e3) / 1e12 / peak}
         del W3
+        # token rows straight from x (no staging rows): the same product
+        dgcfg = mk.make_config(dispatch_ctas=args.dispatch_ctas, n_group=args.n_group, gather=mk.MK_GATHER_DIRECT)
+        dgms = statistics.mean(timed(dgcfg, min(args.steps, 50), 3))
+        line["direct_gather"] = {
+            "ms": dgms, "tflops": w.flop / (dgms / 1e3) / 1e12, "frac_bf16": w.flop / (dgms / 1e3) / 1e12 / peak,
+            "vs_staged": ms_mean / dgms,
+            "workspace_bytes": mk.mk_workspace_size(w.T, w.H, w.F, w.E, w.k, dgcfg),
+            "staged_workspace_bytes": mk.mk_workspace_size(w.T, w.H, w.F, w.E, w.k, cfg)}
         # end to end through the host-buffer entry point
         xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
         lh = torch.from_numpy(l_np).pin_memory()

@@ -1,0 +1,53 @@
+"""Host logic of bench.py that needs no GPU: the clock sampler keeps only the
+samples taken inside the timed region."""
+import datetime
+import os
+import subprocess
+import sys
+import tempfile
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _line(ts, sm, reasons=("Not Active",) * 4):
+    stamp = datetime.datetime.fromtimestamp(ts).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return ", ".join([stamp, "0", str(sm), "2070", "900.00", "0x0", *reasons]) + "\n"
+
+
+def _sampler_with(lines, t0, t1):
+    s = bench.ClockSampler(0)
+    fd, s.path = tempfile.mkstemp(suffix=".csv")
+    os.close(fd)
+    with open(s.path, "w") as f:
+        f.writelines(lines)
+    s.fh = open(os.devnull, "w")
+    s.proc = subprocess.Popen([sys.executable, "-c", "import time; time.sleep(30)"])
+    s.t0, s.t1 = t0, t1
+    return s
+
+
+def test_samples_outside_the_timed_region_are_dropped():
+    t0 = 1_800_000_000.0
+    lines = [_line(t0 - 1.0, 345, ("Not Active", "Not Active", "Not Active", "Active")),  # idle, before
+             _line(t0 + 0.1, 2070), _line(t0 + 0.2, 2055),
+             _line(t0 + 0.3, 2040, ("Not Active", "Not Active", "Not Active", "Active")),
+             _line(t0 + 5.0, 600, ("Active", "Not Active", "Not Active", "Not Active"))]  # after
+    c = _sampler_with(lines, t0, t0 + 1.0).stop()
+    assert c["samples_in_timed_region"] == 3 and c["samples"] == 3
+    assert c["sm_mhz"] == 2055 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]  # the hw_slowdown after the region is not counted
+
+
+def test_all_samples_used_when_none_fell_inside():
+    t0 = 1_800_000_000.0
+    c = _sampler_with([_line(t0 - 2.0, 1900), _line(t0 - 1.0, 2000)], t0, t0 + 0.001).stop()
+    assert c["samples_in_timed_region"] == 0 and c["samples"] == 2 and c["sm_mhz"] == 1950
+
+
+def test_malformed_lines_are_skipped():
+    t0 = 1_800_000_000.0
+    c = _sampler_with(["garbage\n", "[N/A], 0\n", _line(t0 + 0.5, 2070)], t0, t0 + 1.0).stop()
+    assert c["samples"] == 1 and c["sm_mhz"] == 2070

@@ -205,3 +205,52 @@ int mko_expert_rows(const uint16_t* x, const uint16_t* W,
     }
     return MKO_OK;
 }
+
+/* First token of rank r: floor(r*T/R). */
+static int64_t ep_token0(int64_t T, int R, int r) { return (T * (int64_t)r) / R; }
+
+int mko_ep_layout(const int32_t* topk_idx, int64_t T, int E, int k, int R,
+                  int32_t* cnt, int32_t* recv_offsets, int32_t* recv_src) {
+    if (T < 0 || E < 1 || k < 1 || k > E || R < 1 || E % R != 0) return MKO_EARG;
+    if (!cnt || !recv_offsets || (T > 0 && (!topk_idx || !recv_src))) return MKO_EARG;
+    const int epr = E / R;
+    for (int64_t i = 0; i < T * (int64_t)k; ++i)
+        if (topk_idx[i] < 0 || topk_idx[i] >= E) return MKO_EARG;
+
+    /* Step 1: every source rank counts its own entries per expert.
+     * Step 2: the all-gather leaves the whole table on every rank (one
+     * table here stands for the R identical copies). */
+    memset(cnt, 0, sizeof(int32_t) * (size_t)R * (size_t)E);
+    for (int r = 0; r < R; ++r)
+        for (int64_t t = ep_token0(T, R, r); t < ep_token0(T, R, r + 1); ++t)
+            for (int j = 0; j < k; ++j) cnt[(int64_t)r * E + topk_idx[t * k + j]] += 1;
+
+    /* Step 3: receive offsets of the ranks, then the start of every block
+     * (e, r) inside its destination's buffer. */
+    int64_t* block = (int64_t*)malloc(sizeof(int64_t) * (size_t)R * (size_t)E);
+    if (!block) return MKO_EARG;
+    int64_t run = 0;
+    for (int q = 0; q < R; ++q) {
+        recv_offsets[q] = (int32_t)run;
+        for (int e = q * epr; e < (q + 1) * epr; ++e)
+            for (int r = 0; r < R; ++r) {
+                block[(int64_t)r * E + e] = run;
+                run += cnt[(int64_t)r * E + e];
+            }
+    }
+    recv_offsets[R] = (int32_t)run;
+
+    /* Step 4: each source sends its entries in (t, j) order; a block fills
+     * in arrival order. */
+    int bad = 0;
+    for (int r = 0; r < R; ++r)
+        for (int64_t t = ep_token0(T, R, r); t < ep_token0(T, R, r + 1); ++t)
+            for (int j = 0; j < k; ++j) {
+                const int e = topk_idx[t * k + j];
+                const int64_t at = block[(int64_t)r * E + e]++;
+                if (at < 0 || at >= T * (int64_t)k) bad = 1;  /* a block outside the buffers */
+                else recv_src[at] = (int32_t)(t * k + j);
+            }
+    free(block);
+    return bad ? MKO_EARG : MKO_OK;
+}

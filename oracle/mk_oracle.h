@@ -81,6 +81,27 @@ int mko_gated_rows(const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
                    const int32_t* expert_offsets, const int32_t* src_index,
                    const int64_t* rows, int64_t n, double* y);
 
+/* Expert-parallel exchange of the routed entries over R ranks, the setting
+ * of the pages ("mKernel: UCCL fuses NVLink, RDMA and compute ...",
+ * zubnet.ai, para. 2; "mKernel : une bibliotheque ...", lefilia.fr, paras.
+ * 2-3: experts spread over GPUs, tokens sent to the GPU of their expert).
+ * Rank r owns the tokens [T0(r), T0(r+1)) with T0(r) = floor(r*T/R) and the
+ * experts [r*E/R, (r+1)*E/R) (E divisible by R).  The exchange, step by step:
+ *   1. each source rank r counts its own entries (t, j) per expert: cnt[r][e];
+ *   2. the counts are all-gathered, so every rank knows cnt[R][E];
+ *   3. destination q receives, after the rows of the ranks before it
+ *      (recv_offsets[q] = their total), its experts in id order and, inside
+ *      one expert, one block per source rank in rank order:
+ *        block(e, r) = recv_offsets[q] + sum over q's experts e' < e of
+ *                      sum_r' cnt[r'][e'] + sum_{r' < r} cnt[r'][e];
+ *   4. each source r sends its entries in (t, j) order, each to the next
+ *      free row of block(e, r).
+ * Outputs: cnt[R*E] (row r = source r), recv_offsets[R+1], and
+ * recv_src[T*k] = t*k + j of every received row, the ranks' receive buffers
+ * one after another. */
+int mko_ep_layout(const int32_t* topk_idx, int64_t T, int E, int k, int R,
+                  int32_t* cnt, int32_t* recv_offsets, int32_t* recv_src);
+
 /* Number of threads the oracle's parallel loops use. */
 int mko_num_threads(void);
 

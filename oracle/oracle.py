@@ -39,7 +39,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mko_expert_rows.argtypes = [_p, _p, _i64, _int, _int, _int, _int, _p, _p, _p, _i64, _p]
         lib.mko_combine.argtypes = [_p, _p, _p, _i64, _int, _int, _p]
         lib.mko_gated_rows.argtypes = [_p, _p, _p, _i64, _int, _int, _int, _int, _p, _p, _p, _i64, _p]
-        for f in (lib.mko_route, lib.mko_dispatch, lib.mko_expert_rows, lib.mko_combine, lib.mko_gated_rows):
+        lib.mko_ep_layout.argtypes = [_p, _i64, _int, _int, _int, _p, _p, _p]
+        for f in (lib.mko_route, lib.mko_dispatch, lib.mko_expert_rows, lib.mko_combine, lib.mko_gated_rows,
+                  lib.mko_ep_layout):
             f.restype = _int
         lib.mko_num_threads.restype = _int
         _LIBS[path] = lib
@@ -130,6 +132,16 @@ class Oracle:
         out = np.zeros((T, F), dtype=np.float64)
         _check(self.lib.mko_combine(_ptr(y), _ptr(src), _ptr(gate_w), T, k, F, _ptr(out)), "mko_combine")
         return out
+
+    def ep_layout(self, idx: np.ndarray, E: int, R: int):
+        """Expert-parallel exchange over R ranks: (cnt[R,E], recv_offsets[R+1], recv_src[T*k])."""
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        T, k = idx.shape
+        cnt = np.zeros((R, E), dtype=np.int32)
+        roff = np.zeros(R + 1, dtype=np.int32)
+        rsrc = np.zeros(T * k, dtype=np.int32)
+        _check(self.lib.mko_ep_layout(_ptr(idx), T, E, k, R, _ptr(cnt), _ptr(roff), _ptr(rsrc)), "mko_ep_layout")
+        return cnt, roff, rsrc
 
     def full(self, x_bits, logits, W_bits, k, rows=None):
         """Every output of the path; ``rows`` limits the fp64 product to a sample."""

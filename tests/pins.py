@@ -352,6 +352,54 @@ def check_gated_odd_part(o):
     assert np.allclose(hp["y"] - hm["y"], xf * xf, rtol=1e-13, atol=1e-15)
 
 
+# ------------------------------------------------------- expert parallel ----
+
+def _ep_cases():
+    rng = np.random.default_rng(23)
+    for (T, E, k, R) in [(40, 8, 2, 2), (37, 8, 3, 4), (50, 16, 4, 8), (3, 8, 2, 8), (29, 12, 5, 3),
+                         (64, 6, 6, 6), (17, 4, 1, 1)]:
+        yield T, E, k, R, _tie_heavy_logits(rng, T, E, with_neg_inf=False)
+
+
+def check_ep_layout_is_the_global_sort(o):
+    """Experts and tokens owned in contiguous blocks: the ranks' receive
+    buffers, one after another, are the single-device sorted order."""
+    for T, E, k, R, l in _ep_cases():
+        idx, gate = o.route(l, k)
+        offsets, src, _ = o.dispatch(idx, gate, E)
+        cnt, roff, rsrc = o.ep_layout(idx, E, R)
+        assert np.array_equal(rsrc, src), (T, E, k, R)
+        assert np.array_equal(roff, offsets[::E // R]), (T, E, k, R)
+
+
+def check_ep_exchange_structure(o):
+    """Counts by brute force per rank; every received row belongs to one of
+    the destination's experts; inside an expert the sources come in rank
+    order and each source's tokens lie in its own range, ascending."""
+    for T, E, k, R, l in _ep_cases():
+        idx, _ = o.route(l, k)
+        cnt, roff, rsrc = o.ep_layout(idx, E, R)
+        bounds = [T * r // R for r in range(R + 1)]
+        owner = lambda t: max(r for r in range(R) if bounds[r] <= t)  # noqa: E731
+        for r in range(R):
+            for e in range(E):
+                n = sum(1 for t in range(bounds[r], bounds[r + 1]) for j in range(k) if idx[t, j] == e)
+                assert cnt[r, e] == n, (r, e)
+        assert sorted(rsrc.tolist()) == list(range(T * k))
+        epr = E // R
+        for q in range(R):
+            rows = rsrc[roff[q]:roff[q + 1]]
+            es = [int(idx[v // k, v % k]) for v in rows]
+            assert all(q * epr <= e < (q + 1) * epr for e in es), q
+            assert es == sorted(es), q
+            assert roff[q + 1] - roff[q] == cnt[:, q * epr:(q + 1) * epr].sum()
+            for e in set(es):
+                toks = [int(v) // k for v, ee in zip(rows, es) if ee == e]
+                srcs = [owner(t) for t in toks]
+                assert srcs == sorted(srcs), (q, e)
+                assert toks == sorted(toks), (q, e)
+
+
 ALL_CHECKS = [
     check_topk_bruteforce,
     check_topk_special_cases,
@@ -368,4 +416,6 @@ ALL_CHECKS = [
     check_gated_vs_numpy,
     check_gated_zero_gate_projection,
     check_gated_odd_part,
+    check_ep_layout_is_the_global_sort,
+    check_ep_exchange_structure,
 ]

@@ -47,6 +47,13 @@ MUTANTS = {
     "gated_no_up_projection": ("yr[f] = a[f] / (1.0 + exp(-a[f])) * b[f];", "yr[f] = a[f] / (1.0 + exp(-a[f]));"),
     "gated_w3_is_w1": ("const uint16_t* W3e = W3 + (int64_t)e * H * F;", "const uint16_t* W3e = W1 + (int64_t)e * H * F;"),
     "combine_uniform_gate": ("const double g = (double)gate_w[r];", "const double g = 1.0 / k;"),
+    "ep_sources_reversed": ("block[(int64_t)r * E + e] = run;", "block[(int64_t)(R - 1 - r) * E + e] = run;"),
+    "ep_rank_major_blocks": ("for (int e = q * epr; e < (q + 1) * epr; ++e)\n            for (int r = 0; r < R; ++r) {",
+                             "for (int r = 0; r < R; ++r)\n            for (int e = q * epr; e < (q + 1) * epr; ++e) {"),
+    "ep_strided_experts": ("for (int e = q * epr; e < (q + 1) * epr; ++e)", "for (int e = q; e < E; e += R)"),
+    "ep_token_split_ceil": ("static int64_t ep_token0(int64_t T, int R, int r) { return (T * (int64_t)r) / R; }",
+                            "static int64_t ep_token0(int64_t T, int R, int r) { return (T * (int64_t)r + R - 1) / R; }"),
+    "ep_counts_double": ("cnt[(int64_t)r * E + topk_idx[t * k + j]] += 1;", "cnt[(int64_t)r * E + topk_idx[t * k + j]] += 1 + (j > 0);"),
 }
 
 

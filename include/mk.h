@@ -173,6 +173,45 @@ mk_status_t mk_moe_dispatch_gated(const void* x, const float* logits, int T, int
                                   int32_t* expert_offsets, float* gate_w, void* stream, const mk_config_t* cfg,
                                   void* workspace, size_t ws_bytes);
 
+/* Expert parallelism simulated on one GPU.  The pages run MoE
+ * Dispatch+GEMM across GPUs, tokens travelling to the GPU that holds their
+ * expert ("mKernel: UCCL fuses NVLink, RDMA, compute ...", zubnet.ai, para.
+ * 2; "mKernel : une bibliotheque ...", lefilia.fr, paras. 2-3).  Here
+ * `ranks` logical ranks share one launch, each with its own region of the
+ * workspace standing for its device memory.  Rank r owns the tokens
+ * [floor(r*T/R), floor((r+1)*T/R)) and the experts [r*E/R, (r+1)*E/R)
+ * (R = ranks, 1..8, dividing E).  Each rank routes its own tokens, sends
+ * its per-expert count rows to every rank (a flag per source), sends each
+ * routed row to the rank of its expert (a count of arrived rows per tile:
+ * the GEMM starts a tile once every source's rows are in), runs the expert
+ * GEMM for its own experts, and stores every result back into the sending
+ * rank's rows; with `out`, each rank then combines its own tokens once all
+ * their results are back.
+ *
+ * Outputs (device, caller-owned, written):
+ *   y_tok[T*k,F]: the product x[t].W[e] of entry (t, j) at row t*k + j
+ *     (token-major: the sending ranks' return rows, rank r's being rows
+ *     [T0(r)*k, T0(r+1)*k)); bf16, or f32 with MK_OUT_F32.  Not gate-scaled.
+ *   src_index[T*k], gate_w[T*k], expert_offsets[E+1]: the ranks' receive
+ *     buffers one after another, which is exactly the sorted order of
+ *     mk_moe_dispatch_gemm (rank q's rows are [expert_offsets[q*E/R],
+ *     expert_offsets[(q+1)*E/R])).
+ *   out[T,F] (optional, may be NULL): sum_j gate[t,j] * y_tok[t*k+j], fp32
+ *     in slot order, in y_tok's dtype.
+ * Supported: MK_MODE_FUSED, staged rows, single-SM tiles; other choices
+ * return MK_ERR_UNSUPPORTED.  cfg.trace records nothing here.  workspace:
+ * NULL (library cache, zeroed when allocated) or mk_ep_workspace_size()
+ * bytes, 256-byte aligned, zero-filled before its first use, and used by
+ * this entry point only (the others write over its control blocks).  Every rank may
+ * receive up to T*min(k, E/R) rows, so the workspace holds that many
+ * H-wide rows per rank.  Errors as for mk_moe_dispatch_gemm_ex. */
+mk_status_t mk_moe_ep_sim(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,
+                          int ranks, void* y_tok, int32_t* src_index, int32_t* expert_offsets, float* gate_w,
+                          void* out, void* stream, const mk_config_t* cfg, void* workspace, size_t ws_bytes);
+
+/* Workspace bytes mk_moe_ep_sim needs (0 for invalid sizes). */
+size_t mk_ep_workspace_size(int T, int H, int F, int E, int k, int ranks);
+
 /* End-to-end variant: x, logits and the four outputs are HOST buffers
  * (pinned memory gives asynchronous copies); W stays on the device (expert
  * weights are resident).  Copies the inputs in, runs the fused path, copies

@@ -47,6 +47,8 @@ ABI_FUNCTIONS = (
     "mk_moe_dispatch_gated",
     "mk_moe_dispatch_gemm_host",
     "mk_moe_dispatch_gemm_noalloc",
+    "mk_moe_ep_sim",
+    "mk_ep_workspace_size",
     "mk_workspace_size",
     "mk_get_status",
     "mk_last_error_detail",
@@ -128,6 +130,11 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     h.mk_moe_dispatch_gemm_host.restype = _i
     h.mk_moe_dispatch_gemm_noalloc.argtypes = sig + [ctypes.POINTER(mk_config_t)]
     h.mk_moe_dispatch_gemm_noalloc.restype = _i
+    h.mk_moe_ep_sim.argtypes = [_p, _p, _i, _i, _i, _i, _p, _i, _i, _p, _p, _p, _p, _p, _p,
+                                ctypes.POINTER(mk_config_t), _p, ctypes.c_size_t]
+    h.mk_moe_ep_sim.restype = _i
+    h.mk_ep_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+    h.mk_ep_workspace_size.restype = ctypes.c_size_t
     h.mk_workspace_size.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(mk_config_t)]
     h.mk_workspace_size.restype = ctypes.c_size_t
     h.mk_get_status.argtypes = [_p]
@@ -255,6 +262,37 @@ def moe_layer(x, logits, W, k, cfg: mk_config_t | None = None, stream=None, chec
     st = mk_moe_dispatch_gemm_combine(x, logits, T, H, E, k, W, F, o["y_sorted"], o["src_index"],
                                       o["expert_offsets"], o["gate_w"], o["out"], stream, cfg)
     _check(st, "mk_moe_dispatch_gemm_combine")
+    if check:
+        _check(mk_get_status(stream), "device status")
+    return o
+
+
+def mk_moe_ep_sim(x, logits, T, H, E, k, W, F, ranks, y_tok, src_index, expert_offsets, gate_w, out=None,
+                  stream=None, cfg: mk_config_t | None = None, workspace=None, ws_bytes: int = 0) -> int:
+    return int(lib().mk_moe_ep_sim(_ptr(x), _ptr(logits), T, H, E, k, _ptr(W), F, ranks, _ptr(y_tok),
+                                   _ptr(src_index), _ptr(expert_offsets), _ptr(gate_w), _ptr(out), _stream(stream),
+                                   ctypes.byref(cfg) if cfg is not None else None, _ptr(workspace), int(ws_bytes)))
+
+
+def mk_ep_workspace_size(T, H, F, E, k, ranks) -> int:
+    return int(lib().mk_ep_workspace_size(T, H, F, E, k, ranks))
+
+
+def moe_ep_sim(x, logits, W, k, ranks, cfg: mk_config_t | None = None, stream=None, combine=True, check=True):
+    """Expert parallelism over ``ranks`` logical ranks simulated on one GPU;
+    returns ``y_tok[T*k,F]`` (token-major), the receive metadata
+    (``src_index``, ``gate_w``, ``expert_offsets``) and, with ``combine``,
+    ``out[T,F]``."""
+    import torch
+
+    T, H = x.shape
+    E, _, F = W.shape
+    o = alloc_outputs(T, F, E, k, cfg.out_dtype if cfg is not None else MK_OUT_BF16, x.device)
+    o["y_tok"] = o.pop("y_sorted")
+    o["out"] = torch.empty((T, F), dtype=o["y_tok"].dtype, device=x.device) if combine else None
+    st = mk_moe_ep_sim(x, logits, T, H, E, k, W, F, ranks, o["y_tok"], o["src_index"], o["expert_offsets"],
+                       o["gate_w"], o["out"], stream, cfg)
+    _check(st, "mk_moe_ep_sim")
     if check:
         _check(mk_get_status(stream), "device status")
     return o

@@ -27,6 +27,7 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
                          cudaStream_t st);
 cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                            int grid, cudaStream_t st);
+cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& b, int grid, cudaStream_t st);
 cudaError_t set_kernel_attributes();
 cudaError_t fused_max_blocks_per_sm(int* n);
 cudaError_t read_and_clear_error(uint32_t out[4], cudaStream_t st);
@@ -57,6 +58,7 @@ struct WsEntry {
     size_t bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws;
+std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws_ep;  // expert-parallel layout (zeroed whole)
 
 struct HostStage {
     void* ptr = nullptr;
@@ -187,9 +189,9 @@ CUresult encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
 
 // The library's workspace for (device, stream), grown on demand.  The new
 // buffer's bookkeeping part (everything before the staging rows) is zeroed.
-mk_status_t cached_workspace(int dev, cudaStream_t st, size_t need, size_t zero_bytes, void** out) {
+mk_status_t cached_workspace(int dev, cudaStream_t st, size_t need, size_t zero_bytes, void** out, bool ep = false) {
     std::lock_guard<std::mutex> lock(g_mu);
-    WsEntry& w = g_ws[{dev, st}];
+    WsEntry& w = ep ? g_ws_ep[{dev, st}] : g_ws[{dev, st}];
     if (w.bytes < need) {
         if (w.ptr && cudaFreeAsync(w.ptr, st) != cudaSuccess) return MK_ERR_CUDA;
         w.ptr = nullptr;
@@ -199,7 +201,7 @@ mk_status_t cached_workspace(int dev, cudaStream_t st, size_t need, size_t zero_
             w.ptr = nullptr;
             return MK_ERR_CUDA;
         }
-        if (cudaMemsetAsync(w.ptr, 0, zero_bytes, st) != cudaSuccess) return MK_ERR_CUDA;
+        if (cudaMemsetAsync(w.ptr, 0, ep ? grow : zero_bytes, st) != cudaSuccess) return MK_ERR_CUDA;
         w.bytes = grow;
     }
     *out = w.ptr;
@@ -363,6 +365,9 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.xs = reinterpret_cast<uint16_t*>(ws + L.xs);
     p.trace_buf = reinterpret_cast<unsigned long long*>(ws + L.trace);
     p.max_tiles = (rows + p.tile_rows - 1) / p.tile_rows + E;
+    p.ranks = 1;  // routing chunks over [0, T)
+    p.ep_t0[1] = T;
+    p.ep_c0[1] = nch;
 
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof(tmA));
@@ -400,9 +405,158 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     return err == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }
 
+// Expert parallelism simulated with `ranks` logical ranks in one launch.
+mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F, int ranks,
+                   void* y_tok, int32_t* src_index, int32_t* expert_offsets, float* gate_w, void* out, void* stream,
+                   const mk_config_t* cfg_in, void* workspace, size_t ws_bytes) {
+    g_last_info = mk_launch_info_t{};
+    mk_status_t s = validate_sizes(T, H, E, k, F);
+    if (s != MK_OK) return s;
+    if (ranks < 1 || ranks > MAX_RANKS || E % ranks != 0) return MK_ERR_INVALID_ARG;
+    const mk_config_t c = config_or_default(cfg_in);
+    for (int i = 0; i < 4; ++i)
+        if (c.reserved[i] != 0) return MK_ERR_INVALID_ARG;
+    if (c.mma_pair < MK_MMA_AUTO || c.mma_pair > MK_MMA_PAIR) return MK_ERR_INVALID_ARG;
+    if (c.gather < MK_GATHER_AUTO || c.gather > MK_GATHER_DIRECT) return MK_ERR_INVALID_ARG;
+    if (c.mode < MK_MODE_FUSED || c.mode > MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
+    if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
+    if (c.debug_fault != MK_FAULT_NONE && c.debug_fault != MK_FAULT_DROP_TILE_FLAG) return MK_ERR_INVALID_ARG;
+    if (c.dispatch_ctas < 0 || c.grid_ctas < 0 || c.n_group < 0 || c.spin_limit_ns < 0) return MK_ERR_INVALID_ARG;
+    // one fused launch, staged rows, single-SM tiles
+    if (c.mode != MK_MODE_FUSED || c.gather == MK_GATHER_DIRECT || c.mma_pair == MK_MMA_PAIR)
+        return MK_ERR_UNSUPPORTED;
+    if (!expert_offsets || !aligned(expert_offsets, 4)) return MK_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!x || !logits || !W || !y_tok || !src_index || !gate_w) return MK_ERR_INVALID_ARG;
+        if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y_tok, 16) || !aligned(logits, 4) ||
+            !aligned(src_index, 4) || !aligned(gate_w, 4))
+            return MK_ERR_INVALID_ARG;
+        if (out && !aligned(out, 16)) return MK_ERR_INVALID_ARG;
+    }
+    int dev = 0;
+    DevInfo* d = nullptr;
+    if ((s = device_info(&dev, &d)) != MK_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        g_last_info.launches = 0;
+        return cudaMemsetAsync(expert_offsets, 0, size_t(E + 1) * 4, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    }
+
+    int grid = grid_for(*d, c);
+    grid -= grid % ranks;  // whole ranks
+    const int cpr = grid / ranks;
+    if (cpr < 1) return MK_ERR_UNSUPPORTED;
+    const EpLayout L = ep_layout(T, H, E, k, ranks);
+    for (int r = 0; r < ranks; ++r) {
+        const int nt = ep_token0(T, ranks, r + 1) - ep_token0(T, ranks, r);
+        if ((nt + ROUTE_CHUNK - 1) / ROUTE_CHUNK > cpr * MAX_CHUNKS_PER_CTA) return MK_ERR_UNSUPPORTED;
+    }
+    const int bnw = BN;
+    const int nb = (F + bnw - 1) / bnw;
+    // completion counts: a rank's (row, N-block) results in 32 bits
+    if (uint64_t(T) * uint64_t(k) * uint64_t(nb) >= (uint64_t(1) << 32)) return MK_ERR_UNSUPPORTED;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (ws) {
+        if (ws_bytes < L.total || !aligned(ws, 256)) return MK_ERR_WORKSPACE;
+    } else {
+        void* pw = nullptr;
+        if ((s = cached_workspace(dev, st, L.total, L.total, &pw, true)) != MK_OK) return s;
+        ws = static_cast<uint8_t*>(pw);
+    }
+
+    Params p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.logits = logits;
+    p.W = static_cast<const uint16_t*>(W);
+    p.y = y_tok;
+    p.src_index = src_index;
+    p.expert_offsets = expert_offsets;
+    p.gate_w = gate_w;
+    p.T = T;
+    p.H = H;
+    p.F = F;
+    p.E = E;
+    p.k = k;
+    p.out_f32 = c.out_dtype == MK_OUT_F32;
+    p.rows = T * k;
+    p.nch = L.nch;
+    p.nb = nb;
+    p.kblocks = H / BK;
+    p.n_group = c.n_group > 0 ? (c.n_group < nb ? c.n_group : nb) : n_group_for(H, F, nb);
+    p.mode = MK_MODE_FUSED;
+    p.compute = 1;
+    p.tile_rows = BM;
+    {
+        int slots = int((SM_STAGE_END) / (size_t(H) * 2));
+        p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
+    }
+    p.debug_drop_tile = c.debug_fault == MK_FAULT_DROP_TILE_FLAG ? 0 : -1;
+    p.spin_limit_ns = c.spin_limit_ns > 0 ? c.spin_limit_ns : kDefaultSpinNs;
+    p.ctl = reinterpret_cast<Ctl*>(ws + L.ctl);
+    p.topk_idx = reinterpret_cast<int32_t*>(ws + L.topk_idx);
+    p.topk_gate = reinterpret_cast<float*>(ws + L.topk_gate);
+    p.lrank = reinterpret_cast<int32_t*>(ws + L.lrank);
+    p.row_of = reinterpret_cast<int32_t*>(ws + L.row_of);
+    p.combine_out = out;
+    p.trace_buf = reinterpret_cast<unsigned long long*>(ws + L.trace);
+    p.ranks = ranks;
+    int c0 = 0;
+    for (int r = 0; r <= ranks; ++r) {
+        p.ep_t0[r] = ep_token0(T, ranks, r);
+        p.ep_c0[r] = c0;
+        if (r < ranks) c0 += (ep_token0(T, ranks, r + 1) - ep_token0(T, ranks, r) + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    }
+    p.ep = 1;
+    p.ep_cpr = cpr;
+    {
+        const int want = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
+        int per = (want + ranks - 1) / ranks;
+        p.ep_dispatch = per < 1 ? 1 : (per > cpr ? cpr : per);
+    }
+    p.ep_tile_cap = L.tile_cap;
+    p.ep_cap_rows = int(L.cap_rows);
+    CUtensorMap tmA[MAX_RANKS], tmB;
+    std::memset(tmA, 0, sizeof(tmA));
+    std::memset(&tmB, 0, sizeof(tmB));
+    for (int r = 0; r < ranks; ++r) {
+        uint8_t* base = ws + L.rank_base[r];
+        p.ep_ctl[r] = reinterpret_cast<EpCtl*>(ws + L.ep_ctl) + r;
+        p.ep_counts[r] = reinterpret_cast<int32_t*>(base + L.counts_off);
+        p.ep_ready[r] = reinterpret_cast<uint32_t*>(base + L.ready_off);
+        p.ep_recv[r] = reinterpret_cast<uint16_t*>(base + L.recv_off);
+        if (encode_2d(&tmA[r], p.ep_recv[r], uint64_t(H), uint64_t(L.cap_rows), uint64_t(H) * 2, BK, BM) !=
+            CUDA_SUCCESS)
+            return MK_ERR_CUDA;
+    }
+    if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+        return MK_ERR_CUDA;
+
+    const cudaError_t err = launch_ep(p, tmA, tmB, grid, st);
+    g_last_info.launches = 1;
+    g_last_info.grid_ctas = grid;
+    g_last_info.dispatch_ctas = p.ep_dispatch * ranks;
+    g_last_info.n_group = p.n_group;
+    g_last_info.mma_pair = MK_MMA_SINGLE;
+    g_last_info.gather = MK_GATHER_STAGED;
+    g_last_info.workspace_bytes = int64_t(L.total);
+    return err == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+mk_status_t mk_moe_ep_sim(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,
+                          int ranks, void* y_tok, int32_t* src_index, int32_t* expert_offsets, float* gate_w,
+                          void* out, void* stream, const mk_config_t* cfg, void* workspace, size_t ws_bytes) {
+    return run_ep(x, logits, T, H, E, k, W, F, ranks, y_tok, src_index, expert_offsets, gate_w, out, stream, cfg,
+                  workspace, ws_bytes);
+}
+
+size_t mk_ep_workspace_size(int T, int H, int F, int E, int k, int ranks) {
+    if (validate_sizes(T, H, E, k, F) != MK_OK || ranks < 1 || ranks > MAX_RANKS || E % ranks != 0) return 0;
+    return ep_layout(T, H, E, k, ranks).total;
+}
 
 mk_status_t mk_moe_dispatch_gemm_ex(const void* x, const float* logits, int T, int H, int E, int k, const void* W,
                                     int F, void* y_sorted, int32_t* src_index, int32_t* expert_offsets,
@@ -545,6 +699,13 @@ void mk_release_workspace(void) {
         cudaFree(kv.second.ptr);
     }
     g_ws.clear();
+    for (auto& kv : g_ws_ep) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaDeviceSynchronize();
+        cudaFree(kv.second.ptr);
+    }
+    g_ws_ep.clear();
     for (auto& kv : g_host_stage) {
         if (!kv.second.ptr) continue;
         cudaSetDevice(kv.first.first);

@@ -82,6 +82,23 @@ struct Ctl {
 };
 static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");
 
+// Expert-parallel simulation: R logical ranks inside one GPU.  Each rank
+// owns a region of the workspace (its "device memory") and this control
+// block; other ranks touch them only through the exchange: count rows and
+// their flags, received rows and their arrival counts, returned results and
+// their completion count.
+constexpr int MAX_RANKS = 8;
+struct EpCtl {
+    uint32_t routed;                // this rank's CTAs whose count rows are sent
+    uint32_t scattered;             // this rank's CTAs whose receive metadata is written
+    uint32_t next_send;             // this rank's send queue (as a source)
+    uint32_t next_item;             // work queue over this rank's experts
+    uint32_t ret_done;              // (row, N-block) results stored into this rank's return rows
+    uint32_t cnt_flag[MAX_RANKS];   // source r's count rows are in this rank's table copy
+    uint32_t pad[64 - 5 - MAX_RANKS];
+};
+static_assert(sizeof(EpCtl) == 256, "rank control block is 256 bytes");
+
 enum Mode : int { MODE_FUSED = 0, MODE_UNFUSED = 1, MODE_DISPATCH_ONLY = 2 };
 
 // Error sites recorded with a device error (mk_last_error_detail()).
@@ -100,6 +117,9 @@ enum Site : int {
     SITE_ROW_TOTAL = 12,
     SITE_DRAIN = 13,
     SITE_BAR_COMPUTED = 14,
+    SITE_EP_COUNTS = 15,
+    SITE_EP_SCATTERED = 16,
+    SITE_EP_RETURNED = 17,
 };
 
 enum ErrCode : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_FAULT = 2 };
@@ -147,6 +167,24 @@ struct Params {
     uint16_t* xs;            // [T*k,H] bf16 staging
     unsigned long long* trace_buf;  // [grid][TRACE_SLOTS]
     int max_tiles;
+    // token ranges of the routing chunks: rank r's tokens [ep_t0[r], ep_t0[r+1])
+    // are split into the chunks [ep_c0[r], ep_c0[r+1]) (one rank, [0, T), when
+    // not simulating expert parallelism)
+    int ranks;
+    int ep_t0[MAX_RANKS + 1];
+    int ep_c0[MAX_RANKS + 1];
+    // expert-parallel simulation (ep = 1): rank r also owns the experts
+    // [r*E/R, (r+1)*E/R) and the CTAs [r*ep_cpr, (r+1)*ep_cpr), the first
+    // ep_dispatch of which send before they compute
+    int ep;
+    int ep_cpr;
+    int ep_dispatch;
+    int ep_tile_cap;                 // tile counters per rank
+    int ep_cap_rows;                 // receive rows per rank
+    EpCtl* ep_ctl[MAX_RANKS];
+    int32_t* ep_counts[MAX_RANKS];   // each rank's copy of the count table [nch][E]
+    uint32_t* ep_ready[MAX_RANKS];   // rows arrived per tile of the rank's experts
+    uint16_t* ep_recv[MAX_RANKS];    // received rows [cap][H] bf16 (the GEMM's A operand)
 };
 
 // Workspace carve-up, shared by the size query and the launcher.
@@ -174,6 +212,53 @@ inline WsLayout ws_layout(int T, int H, int E, int k, bool staging = true, int g
     L.ready = o;      o = ws_align(o + max_tiles * 4);
     L.trace = o;      o = ws_align(o + size_t(grid) * TRACE_SLOTS * 8);
     L.xs = o;         o = ws_align(o + (staging ? rows * size_t(H) * 2 : 0));
+    L.total = o;
+    return L;
+}
+
+// Expert-parallel workspace: a head (control block, the ranks' control
+// blocks, routing results of the ranks' own tokens, trace) and one region
+// per rank.  The rank control blocks sit at fixed offsets whatever the
+// sizes, so a cached workspace reused with other sizes or rank counts still
+// finds them zeroed (the last CTA of every call leaves them so).  A rank
+// receives at most T * min(k, E/R) rows: every token brings at most one row
+// per expert, and each of the rank's E/R experts is one of its k.
+struct EpLayout {
+    size_t ctl, ep_ctl, topk_idx, topk_gate, lrank, row_of, trace;
+    size_t rank_base[MAX_RANKS], rank_bytes;
+    size_t counts_off, ready_off, recv_off;  // inside a rank region
+    int nch, tile_cap;
+    size_t cap_rows;
+    size_t total;
+};
+
+inline int ep_token0(int T, int R, int r) { return int((int64_t(T) * r) / R); }
+
+inline EpLayout ep_layout(int T, int H, int E, int k, int R, int grid = MAX_GRID) {
+    EpLayout L{};
+    const size_t rows = size_t(T) * k;
+    int nch = 0;
+    for (int r = 0; r < R; ++r) nch += (ep_token0(T, R, r + 1) - ep_token0(T, R, r) + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    L.nch = nch;
+    L.cap_rows = size_t(T) * size_t(k < E / R ? k : E / R);
+    L.tile_cap = int((L.cap_rows + BM - 1) / BM) + E / R;
+    size_t o = 0;
+    L.ctl = o;        o = ws_align(o + sizeof(Ctl));
+    L.ep_ctl = o;     o = ws_align(o + MAX_RANKS * sizeof(EpCtl));
+    L.topk_idx = o;   o = ws_align(o + rows * 4);
+    L.topk_gate = o;  o = ws_align(o + rows * 4);
+    L.lrank = o;      o = ws_align(o + rows * 4);
+    L.row_of = o;     o = ws_align(o + rows * 4);
+    L.trace = o;      o = ws_align(o + size_t(grid) * TRACE_SLOTS * 8);
+    size_t q = 0;
+    L.counts_off = q; q = ws_align(q + size_t(nch) * E * 4);
+    L.ready_off = q;  q = ws_align(q + size_t(L.tile_cap) * 4);
+    L.recv_off = q;   q = ws_align(q + L.cap_rows * size_t(H) * 2);
+    L.rank_bytes = q;
+    for (int r = 0; r < R; ++r) {
+        L.rank_base[r] = o;
+        o += q;
+    }
     L.total = o;
     return L;
 }

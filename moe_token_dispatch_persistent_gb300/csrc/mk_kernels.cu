@@ -158,6 +158,8 @@ struct CtrlSmem {
     int32_t tile_start[MAX_E + 1];
     int32_t item_start[MAX_E + 1];
     int32_t tot[MAX_E];
+    int32_t ep_pre[MAX_E];  // expert parallel: rows of each expert sent by earlier ranks
+    int32_t ep_cnt[MAX_E];  //                  and by this CTA's rank
 };
 static_assert(sizeof(CtrlSmem) <= SM_CTRL_BYTES, "control smem too large");
 static_assert(offsetof(CtrlSmem, info) % 16 == 0, "info slots must allow 16-byte stores");
@@ -171,12 +173,25 @@ __device__ __forceinline__ CtrlSmem* ctrl() { return reinterpret_cast<CtrlSmem*>
 
 // ------------------------------------------------------------ phase R ------
 
+// Tokens [t0, t1) of routing chunk c: rank r's tokens [ep_t0[r], ep_t0[r+1])
+// are cut into chunks of ROUTE_CHUNK from the rank's first token (one rank:
+// chunk c covers [c*ROUTE_CHUNK, ...)).  Chunks in id order cover the tokens
+// in order, so the sorted order does not depend on where chunks begin.
+__device__ __forceinline__ void chunk_tokens(const Params& p, int c, int& t0, int& t1) {
+    int r = 0;
+    while (r + 1 < p.ranks && p.ep_c0[r + 1] <= c) ++r;
+    t0 = p.ep_t0[r] + (c - p.ep_c0[r]) * ROUTE_CHUNK;
+    t1 = min(t0 + ROUTE_CHUNK, p.ep_t0[r + 1]);
+}
+
 // Key order of the router: (value desc, expert id asc).
 __device__ __forceinline__ bool beats(float v, int e, float u, int f) { return v > u || (v == u && e < f); }
 
 // Route one chunk of ROUTE_CHUNK tokens: top-k + gates, per-chunk histogram,
 // and each (t, j)'s rank among the chunk's entries of the same expert in
-// (t, j) order.  Whole CTA.
+// (t, j) order.  Whole CTA.  The chunk's count row goes to the count table,
+// or, simulating expert parallelism, to every rank's copy of it (the
+// all-gather of the counts).
 __device__ void route_chunk(const Params& p, int c) {
     uint8_t* s = smem_base();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,8 +199,10 @@ __device__ void route_chunk(const Params& p, int c) {
     int* sidx = reinterpret_cast<int*>(s + RT_IDX) + warp * 32 * MAX_K;
     int* slr = reinterpret_cast<int*>(s + RT_LRANK) + warp * 32 * MAX_K;
     int* wcnt = reinterpret_cast<int*>(s + RT_WCNT);
-    const int E = p.E, k = p.k, T = p.T;
-    const int tbase = c * ROUTE_CHUNK + warp * 32;
+    const int E = p.E, k = p.k;
+    int tc0, T;  // the chunk's tokens [tc0, T)
+    chunk_tokens(p, c, tc0, T);
+    const int tbase = tc0 + warp * 32;
     const int t = tbase + lane;
 
     for (int e = lane; e < E; e += 32) wcnt[warp * MAX_E + e] = 0;
@@ -294,7 +311,11 @@ __device__ void route_chunk(const Params& p, int c) {
             wcnt[w * MAX_E + e] = run;
             run += v;
         }
-        p.counts[size_t(c) * E + e] = run;
+        if (p.ep) {
+            for (int q = 0; q < p.ranks; ++q) p.ep_counts[q][size_t(c) * E + e] = run;
+        } else {
+            p.counts[size_t(c) * E + e] = run;
+        }
     }
     __syncthreads();
     if (t < T) {
@@ -357,12 +378,16 @@ __device__ void build_tables(const Params& p, CtrlSmem* cs) {
     }
 }
 
-// Totals from the full counts table; for the CTA's own chunks, the column
-// prefix (rows of earlier chunks) is kept in smem as the chunk's bases.
-__device__ void scan_counts(const Params& p, CtrlSmem* cs, bool keep_bases) {
+// Totals from the full counts table; for the CTA's own chunks (c_first,
+// c_first + c_stride, ... below c_end) the column prefix (rows of earlier
+// chunks) is kept in smem as the chunk's bases.  With src_rank >= 0 the
+// per-expert rows of the chunks before that rank's (ep_pre) and of its own
+// chunks (ep_cnt) are kept too: where its rows sit inside each expert.
+__device__ void scan_counts(const Params& p, CtrlSmem* cs, const int32_t* counts, bool keep_bases, int c_first,
+                            int c_stride, int c_end, int src_rank) {
     int* sbase = reinterpret_cast<int*>(smem_base() + RT_BASES);
     int* scnt = reinterpret_cast<int*>(smem_base());  // routing scratch is dead by now
-    const int E = p.E, nch = p.nch, grid = gridDim.x;
+    const int E = p.E, nch = p.nch;
     const int total = nch * E;
     const bool in_smem = total <= RT_BASES / 4;
     if (in_smem) {
@@ -372,7 +397,7 @@ __device__ void scan_counts(const Params& p, CtrlSmem* cs, bool keep_bases) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = b0 + j * NTHREADS + threadIdx.x;
-                v[j] = i < total ? __ldcg(p.counts + i) : 0;
+                v[j] = i < total ? __ldcg(counts + i) : 0;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -382,25 +407,35 @@ __device__ void scan_counts(const Params& p, CtrlSmem* cs, bool keep_bases) {
         }
         __syncthreads();
     }
+    const int s_lo = src_rank >= 0 ? p.ep_c0[src_rank] : 0;
+    const int s_hi = src_rank >= 0 ? p.ep_c0[src_rank + 1] : 0;
     for (int e = threadIdx.x; e < E; e += NTHREADS) {
-        int run = 0, m = 0;
-        int mine = blockIdx.x;
+        int run = 0, m = 0, pre = 0, upto = 0;
+        int mine = c_first;
         for (int c = 0; c < nch; ++c) {
-            if (keep_bases && c == mine) {
+            if (keep_bases && c == mine && c < c_end) {
                 sbase[m * MAX_E + e] = run;
                 ++m;
-                mine += grid;
+                mine += c_stride;
             }
-            run += in_smem ? scnt[c * E + e] : __ldcg(p.counts + size_t(c) * E + e);
+            if (c == s_lo) pre = run;
+            if (c == s_hi) upto = run;
+            run += in_smem ? scnt[c * E + e] : __ldcg(counts + size_t(c) * E + e);
         }
         cs->tot[e] = run;
+        if (src_rank >= 0) {
+            if (s_lo >= nch) pre = run;
+            if (s_hi >= nch) upto = run;
+            cs->ep_pre[e] = pre;
+            cs->ep_cnt[e] = upto - pre;
+        }
     }
     __syncthreads();
     build_tables(p, cs);
     __syncthreads();
     if (keep_bases) {
         int m = 0;
-        for (int c = blockIdx.x; c < nch; c += grid, ++m)
+        for (int c = c_first; c < c_end; c += c_stride, ++m)
             for (int e = threadIdx.x; e < E; e += NTHREADS) sbase[m * MAX_E + e] += cs->offs[e];
     }
     __syncthreads();
@@ -408,9 +443,10 @@ __device__ void scan_counts(const Params& p, CtrlSmem* cs, bool keep_bases) {
 
 // Scatter src_index / gate_w for (t, j) entries of chunk c (bases in smem).
 __device__ void scatter_chunk(const Params& p, int c, const int* cbase, const WaitCtx& w) {
-    const int k = p.k, T = p.T;
-    const int t0 = c * ROUTE_CHUNK;
-    const int n = min(ROUTE_CHUNK, T - t0) * k;
+    const int k = p.k;
+    int t0, t1;
+    chunk_tokens(p, c, t0, t1);
+    const int n = (t1 - t0) * k;
     constexpr int U = 4;  // entries per thread per batch: loads issued before the stores
     for (int i0 = threadIdx.x; i0 < n; i0 += NTHREADS * U) {
         int e[U], lr[U];
@@ -517,6 +553,81 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, uint32_t flag, const 
     bulk_wait_all();
 }
 
+// Expert-parallel send role of source rank `src` (warp 0): the rank walks
+// the destination tiles (tile i of every rank before tile i + 1 of any, so
+// each destination's first tiles fill first) and, for each tile that holds
+// rows of its own tokens, copies those rows x -> smem -> the destination's
+// receive buffer with 1-D bulk copies, then adds their number to the tile's
+// arrival count (release).  Inside one expert the rows of a source are one
+// contiguous range (sorted by token), so a tile takes one range per source;
+// the tile is complete when its count reaches its row count.
+__device__ void send_role(const Params& p, CtrlSmem* cs, int src, const WaitCtx& w) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp != 0) return;
+    uint8_t* s = smem_base();
+    const uint32_t row_bytes = uint32_t(p.H) * 2u;
+    const int nslot = p.gather_slots;
+    const int R = p.ranks, epr = p.E / R;
+    int max_tiles = 0;
+    for (int q = 0; q < R; ++q)
+        max_tiles = max(max_tiles, cs->tile_start[(q + 1) * epr] - cs->tile_start[q * epr]);
+    const int t_lo = p.ep_t0[src], t_hi = p.ep_t0[src + 1];
+    uint32_t ph = 0;
+    bool ok = true;
+    while (ok) {
+        int sq = 0;
+        if (lane == 0) sq = int(atom_add_relaxed_u32(&p.ep_ctl[src]->next_send, 1u));
+        sq = __shfl_sync(0xffffffffu, sq, 0);
+        if (sq >= R * max_tiles) break;
+        const int q = sq % R, i = sq / R;
+        const int tile_lo = cs->tile_start[q * epr];
+        const int tile = tile_lo + i;
+        if (tile >= cs->tile_start[(q + 1) * epr]) continue;
+        const int e = find_expert(cs->tile_start, p.E, tile);
+        const int row0 = cs->offs[e] + (tile - cs->tile_start[e]) * p.tile_rows;
+        const int row1 = min(row0 + p.tile_rows, cs->offs[e + 1]);
+        const int lo = max(row0, cs->offs[e] + cs->ep_pre[e]);
+        const int hi = min(row1, cs->offs[e] + cs->ep_pre[e] + cs->ep_cnt[e]);
+        if (lo >= hi) continue;
+        uint16_t* recv = p.ep_recv[q];
+        const int recv0 = cs->offs[q * epr];  // first sorted row of rank q
+        if (lane < nslot) {
+            uint8_t* slot = s + size_t(lane) * row_bytes;
+            for (int r = lo + lane; r < hi && ok; r += nslot) {
+                const int src_t = __ldcg(p.src_index + r) / p.k;
+                if (src_t < t_lo || src_t >= t_hi) {
+                    record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(r));
+                    raise_abort(w);
+                    ok = false;
+                    break;
+                }
+                bulk_wait_read<0>();
+                mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
+                bulk_load(slot, p.x + size_t(src_t) * p.H, row_bytes, &cs->gbar[lane]);
+                if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
+                    ok = false;
+                    WaitCtx shortw{nullptr, 0u, 2000000LL};
+                    wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
+                }
+                ph ^= 1u;
+                if (ok) {
+                    bulk_store(recv + size_t(r - recv0) * p.H, slot, row_bytes);
+                    bulk_commit();
+                }
+            }
+            bulk_wait_all();
+            fence_proxy_async();
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0 && ok && tile != p.debug_drop_tile) {
+            __threadfence();
+            atom_add_acq_rel_u32(p.ep_ready[q] + (tile - tile_lo), uint32_t(hi - lo));
+        }
+        if (aborted(w)) break;
+    }
+    bulk_wait_all();
+}
+
 // Unfused path: push-gather of chunk c (every entry to its destination row).
 __device__ void push_gather_chunk(const Params& p, int c, CtrlSmem* cs, uint32_t& ph, const WaitCtx& w) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -524,9 +635,10 @@ __device__ void push_gather_chunk(const Params& p, int c, CtrlSmem* cs, uint32_t
     uint8_t* s = smem_base();
     const uint32_t row_bytes = uint32_t(p.H) * 2u;
     const int nslot = p.gather_slots;
-    const int k = p.k, T = p.T;
-    const int t0 = c * ROUTE_CHUNK;
-    const int n = min(ROUTE_CHUNK, T - t0) * k;
+    const int k = p.k;
+    int t0, t1;
+    chunk_tokens(p, c, t0, t1);
+    const int n = (t1 - t0) * k;
     if (lane < nslot) {
         uint8_t* slot = s + size_t(lane) * row_bytes;
         for (int i = lane; i < n; i += nslot) {
@@ -742,14 +854,37 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
     __syncwarp();
 }
 
+// Where a compute role takes its work: items [lo, hi) of the work order,
+// claimed through the counter `next`; the A operand's tensor map starts at
+// sorted row a_row0.  With `arrived` (expert parallel) tile g is ready once
+// arrived[g - tile_lo] reaches its row count.
+struct WorkQueue {
+    uint32_t* next;
+    int lo, hi;
+    int a_row0;
+    const uint32_t* arrived;
+    int tile_lo;
+};
+
+// The single-device queue: every work item, A operand over all sorted rows.
+__device__ __forceinline__ WorkQueue whole_queue(const Params& p, const CtrlSmem* cs) {
+    return WorkQueue{&p.ctl->next_item, 0, cs->item_start[p.E], 0, nullptr, 0};
+}
+
+// Sending rank of token t (expert parallel).
+__device__ __forceinline__ int rank_of_token(const Params& p, int t) {
+    int r = 0;
+    while (r + 1 < p.ranks && p.ep_t0[r + 1] <= t) ++r;
+    return r;
+}
+
 // Warp-specialised expert GEMM over work items (tile, N-block) taken from the
-// shared queue until it is empty.  wait_ready: spin on the tile's flag first.
+// queue until it is empty.  wait_ready: spin on the tile's flag first.
 __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmB3,
-                             CtrlSmem* cs,
+                             CtrlSmem* cs, const WorkQueue& wq,
                              bool wait_ready, uint32_t flag, const WaitCtx& w) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* s = smem_base();
-    const int total_items = cs->item_start[p.E];
     // Waits inside the pipeline only stall because something upstream (a
     // tile flag, a barrier) stalls: they get twice the limit, so the wait
     // that times out and is recorded is the one at the root.
@@ -763,21 +898,21 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             uint32_t stage = 0, phase = 0;
             uint32_t issued_par = 0, issued_any = 0;  // per-stage bit: parity of the last issue
             bool ok = true;
-            uint32_t next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+            uint32_t next = atom_add_relaxed_u32(wq.next, 1u);
             const int ntiles = cs->tile_start[p.E];
             for (uint32_t it = 0; ok; ++it) {
-                const int item = int(next);
+                const int item = wq.lo + int(next);
                 const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
                 if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
                     ok = false;
                     break;
                 }
-                if (item >= total_items) {
+                if (item >= wq.hi) {
                     cs->info[slot].e = -1;
                     mbar_arrive(&cs->info_full[slot]);
                     break;
                 }
-                next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);  // prefetch the next item
+                next = atom_add_relaxed_u32(wq.next, 1u);  // prefetch the next item
                 Info inf;
                 int gtile;
                 decode_item(p, cs, item, inf, gtile);
@@ -794,7 +929,14 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 }
                 cs->info[slot] = inf;
                 mbar_arrive(&cs->info_full[slot]);
-                if (wait_ready) {
+                if (wq.arrived) {
+                    // every source's rows of this tile have landed
+                    if (!wait_geq(wq.arrived + (gtile - wq.tile_lo), uint32_t(inf.nrows), w, SITE_TILE_READY)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async();
+                } else if (wait_ready) {
                     // one acquire per item until every tile is known to be in
                     if (ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles)) {
                         wait_ready = false;
@@ -821,7 +963,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
                     uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
-                    tma_load_2d(a, tmA, kb * BK, inf.row0, fb);
+                    tma_load_2d(a, tmA, kb * BK, inf.row0 - wq.a_row0, fb);
                     if (p.gated) {
                         // 128 columns of W1 into the first half of the B stage, of W3 into the second
 #pragma unroll
@@ -935,7 +1077,10 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             tc_fence_after();
             const int rloc = quad * 32 + lane;
             const bool rowok = rloc < inf.nrows;
-            const size_t row = size_t(inf.row0) + rloc;
+            // expert parallel: the result goes back to the sending rank, into
+            // its return rows in (t, j) order
+            const int ep_q = (p.ep && rowok) ? __ldcg(p.src_index + inf.row0 + rloc) : -1;
+            const size_t row = p.ep ? size_t(ep_q < 0 ? 0 : ep_q) : size_t(inf.row0) + rloc;
             const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + acc * BN;
             if (p.gated) {
                 const int n0 = inf.nbk * GATED_BN;
@@ -967,6 +1112,15 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     if (rowok) store_row32(p, row, col, r);
                 }
             }
+            if (p.ep) {
+                // one count per (warp, sending rank): this item's rows are stored
+                const int src = ep_q >= 0 ? rank_of_token(p, ep_q / p.k) : -1;
+                __threadfence();  // this lane's stores before the count that publishes them
+                __syncwarp();
+                const uint32_t peers = __match_any_sync(0xffffffffu, src);
+                if (src >= 0 && lane == __ffs(peers) - 1)
+                    atom_add_acq_rel_u32(&p.ep_ctl[src]->ret_done, uint32_t(__popc(peers)));
+            }
             tc_fence_before();
             mbar_arrive(&cs->acc_empty[acc]);
             acc ^= 1u;
@@ -977,24 +1131,25 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
 
 // ------------------------------------------------------------ combine ------
 
-// out[t,:] = sum_j gate[t,j] * y_sorted[row_of(t,j), :], fp32 in slot order
-// (deterministic, no atomics), stored in y_sorted's dtype.  Tokens are
-// spread over CTAs [first, first + stride, ...).  The pass is HBM-bound, so
-// each thread first issues 16 independent 16-byte loads (16/K column
-// vectors of the token's K rows) and only then accumulates and stores.
+// out[t,:] = sum_j gate[t,j] * y[row of (t,j), :], fp32 in slot order
+// (deterministic, no atomics), stored in y's dtype.  y is y_sorted (row of
+// (t, j) from row_of) or, expert parallel, the token-major return rows (row
+// t*k + j).  Tokens t_first, t_first + stride, ... below t_end.  The pass is
+// HBM-bound, so each thread first issues 16 independent 16-byte loads (16/K
+// column vectors of the token's K rows) and only then accumulates and stores.
 template <int K>
-__device__ void combine_tokens_k(const Params& p, int first, int stride) {
+__device__ void combine_tokens_k(const Params& p, int t_first, int t_end, int stride) {
     constexpr int U = 16 / K;  // 16-byte vectors per thread per pass
     const int F = p.F;
     const bool f32 = p.out_f32 != 0;
     const int nvec = f32 ? F / 4 : F / 8;
-    for (int t = first; t < p.T; t += stride) {
+    for (int t = t_first; t < t_end; t += stride) {
         const uint4* src[K];
         float g[K];
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             // in range even if an error path left a row unrecorded
-            const int r = min(max(__ldcg(p.row_of + size_t(t) * K + j), 0), p.rows - 1);
+            const int r = p.ep ? t * K + j : min(max(__ldcg(p.row_of + size_t(t) * K + j), 0), p.rows - 1);
             src[j] = f32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(p.y) + size_t(r) * F)
                          : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.y) + size_t(r) * F);
             g[j] = __ldcg(p.topk_gate + size_t(t) * K + j);
@@ -1051,16 +1206,16 @@ __device__ void combine_tokens_k(const Params& p, int first, int stride) {
     }
 }
 
-__device__ void combine_tokens(const Params& p, int first, int stride) {
+__device__ void combine_tokens(const Params& p, int t_first, int t_end, int stride) {
     switch (p.k) {
-        case 1: combine_tokens_k<1>(p, first, stride); break;
-        case 2: combine_tokens_k<2>(p, first, stride); break;
-        case 3: combine_tokens_k<3>(p, first, stride); break;
-        case 4: combine_tokens_k<4>(p, first, stride); break;
-        case 5: combine_tokens_k<5>(p, first, stride); break;
-        case 6: combine_tokens_k<6>(p, first, stride); break;
-        case 7: combine_tokens_k<7>(p, first, stride); break;
-        default: combine_tokens_k<8>(p, first, stride); break;
+        case 1: combine_tokens_k<1>(p, t_first, t_end, stride); break;
+        case 2: combine_tokens_k<2>(p, t_first, t_end, stride); break;
+        case 3: combine_tokens_k<3>(p, t_first, t_end, stride); break;
+        case 4: combine_tokens_k<4>(p, t_first, t_end, stride); break;
+        case 5: combine_tokens_k<5>(p, t_first, t_end, stride); break;
+        case 6: combine_tokens_k<6>(p, t_first, t_end, stride); break;
+        case 7: combine_tokens_k<7>(p, t_first, t_end, stride); break;
+        default: combine_tokens_k<8>(p, t_first, t_end, stride); break;
     }
 }
 
@@ -1357,6 +1512,17 @@ __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
             c->bar_computed = 0;
             c->abort = 0;
             c->epoch = c->epoch + 1u;  // calls completed on this workspace
+            if (p.ep) {
+                for (int r = 0; r < p.ranks; ++r) {
+                    EpCtl* q = p.ep_ctl[r];
+                    q->routed = 0;
+                    q->scattered = 0;
+                    q->next_send = 0;
+                    q->next_item = 0;
+                    q->ret_done = 0;
+                    for (int s = 0; s < MAX_RANKS; ++s) q->cnt_flag[s] = 0;
+                }
+            }
             c->exit_count = 0;
             __threadfence();
         }
@@ -1400,7 +1566,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (ok) {
         // phase S
-        scan_counts(p, cs, true);
+        scan_counts(p, cs, p.counts, true, blockIdx.x, gridDim.x, p.nch, -1);
         if (blockIdx.x == 0)
             for (int e = threadIdx.x; e <= p.E; e += NTHREADS) p.expert_offsets[e] = cs->offs[e];
         if (threadIdx.x == 0 && cs->offs[p.E] != p.rows) {
@@ -1437,7 +1603,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (cs->bcast[2]) {
             stamp(p, 6);
             if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, true, flag, w);
-            else compute_role(p, &tmA, &tmB, &tmB3, cs, !p.direct, flag, w);
+            else compute_role(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), !p.direct, flag, w);
             stamp(p, 7);
         }
     }
@@ -1451,10 +1617,129 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         __syncthreads();
         stamp(p, 8);
-        if (cs->bcast[3]) combine_tokens(p, blockIdx.x, gridDim.x);
+        if (cs->bcast[3]) combine_tokens(p, blockIdx.x, p.T, gridDim.x);
         stamp(p, 9);
     }
     cta_teardown<PAIR>(p, cs, p.compute != 0);
+}
+
+// Expert-parallel simulation: R logical ranks in one cooperative launch
+// (ranks that wait on one another must be resident together), the CTAs
+// [r*cpr, (r+1)*cpr) playing rank r.  Each rank routes its own tokens and
+// sends its count rows to every rank (a flag per source at each
+// destination); once it holds every rank's rows it scans its copy of the
+// table, writes the receive metadata of its own rows, sends the rows to the
+// ranks that own their experts (arrival counts per tile), runs the GEMM on
+// its own experts' tiles as they complete, stores every result back into
+// the sending rank's return rows (a completion count per sending rank), and
+// finally combines its own tokens once all their results are back.
+struct EpMaps {
+    CUtensorMap a[MAX_RANKS];  // A operand of each rank: its received rows
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    mk_ep_kernel(const Params p, const __grid_constant__ EpMaps maps, const __grid_constant__ CUtensorMap tmB) {
+    CtrlSmem* cs = ctrl();
+    const uint32_t flag = 1u;
+    const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
+    const int R = p.ranks, cpr = p.ep_cpr, epr = p.E / R;
+    const int rank = int(blockIdx.x) / cpr, b = int(blockIdx.x) - rank * cpr;
+    EpCtl* me = p.ep_ctl[rank];
+    stamp(p, 0);
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&maps.a[rank]);
+        tma_prefetch_desc(&tmB);
+    }
+    cta_setup<0>(cs, true, false);
+    // This rank's arrival counts start at 0: sources add to them only once
+    // they hold this rank's count rows, which it sends after this.
+    for (int i = b * NTHREADS + threadIdx.x; i < p.ep_tile_cap; i += cpr * NTHREADS) p.ep_ready[rank][i] = 0u;
+
+    // phase R: own tokens; each chunk's count row goes to every rank
+    for (int c = p.ep_c0[rank] + b; c < p.ep_c0[rank + 1]; c += cpr) route_chunk(p, c);
+    stamp(p, 1);
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t before = atom_add_acq_rel_u32(&me->routed, 1u);
+        if (before == uint32_t(cpr - 1))  // the rank's last CTA raises its flag at every rank
+            for (int q = 0; q < R; ++q) st_release_u32(&p.ep_ctl[q]->cnt_flag[rank], 1u);
+        for (int s = 0; s < R && ok; ++s) ok = wait_eq(&me->cnt_flag[s], 1u, w, SITE_EP_COUNTS);
+        cs->bcast[0] = ok;
+    }
+    __syncthreads();
+    ok = cs->bcast[0] != 0;
+    stamp(p, 2);
+
+    if (ok) {
+        // phase S on this rank's copy of the table
+        scan_counts(p, cs, p.ep_counts[rank], true, p.ep_c0[rank] + b, cpr, p.ep_c0[rank + 1], rank);
+        if (blockIdx.x == 0)
+            for (int e = threadIdx.x; e <= p.E; e += NTHREADS) p.expert_offsets[e] = cs->offs[e];
+        if (threadIdx.x == 0 && cs->offs[p.E] != p.rows) {
+            record_error(ERR_FAULT, SITE_ROW_TOTAL, uint32_t(cs->offs[p.E]));
+            raise_abort(w);
+        }
+        // Every rank's rows fit its receive buffer (T*min(k, E/R) rows; only
+        // repeated experts in one token, from logits outside the contract,
+        // could exceed it).  Every CTA holds the same tables, so all agree.
+        bool fits = true;
+        for (int q = 0; q < R; ++q)
+            if (cs->offs[(q + 1) * epr] - cs->offs[q * epr] > p.ep_cap_rows) fits = false;
+        if (!fits) {
+            if (threadIdx.x == 0) {
+                record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(cs->offs[p.E]));
+                raise_abort(w);
+            }
+            cta_teardown<0>(p, cs, true);
+            return;
+        }
+        // receive metadata of the rank's own rows, written at their destinations
+        const int* sbase = reinterpret_cast<const int*>(smem_base() + RT_BASES);
+        int m = 0;
+        for (int c = p.ep_c0[rank] + b; c < p.ep_c0[rank + 1]; c += cpr, ++m)
+            scatter_chunk(p, c, sbase + m * MAX_E, w);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atom_add_acq_rel_u32(&me->scattered, 1u);
+        }
+        stamp(p, 3);
+        if (b < p.ep_dispatch) {
+            // the send role reads the metadata every CTA of its rank wrote
+            if (threadIdx.x == 0) cs->bcast[1] = wait_geq(&me->scattered, uint32_t(cpr), w, SITE_EP_SCATTERED);
+            fence_proxy_async_shared();  // generic smem use (routing) before bulk copies into it
+            __syncthreads();
+            stamp(p, 4);
+            if (cs->bcast[1]) send_role(p, cs, rank, w);
+            __syncthreads();
+            stamp(p, 5);
+        }
+        if (threadIdx.x == 0) cs->bcast[2] = !aborted(w);
+        fence_proxy_async_shared();  // generic/bulk smem use before TMA writes into it
+        __syncthreads();
+        if (cs->bcast[2]) {
+            stamp(p, 6);
+            const int e0 = rank * epr, e1 = e0 + epr;
+            const WorkQueue wq{&me->next_item, cs->item_start[e0], cs->item_start[e1], cs->offs[e0],
+                               p.ep_ready[rank], cs->tile_start[e0]};
+            compute_role(p, &maps.a[rank], &tmB, nullptr, cs, wq, false, flag, w);
+            stamp(p, 7);
+        }
+        if (p.combine_out) {
+            // reduce: every result row of the rank's tokens is back
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const uint32_t need = uint32_t(p.ep_t0[rank + 1] - p.ep_t0[rank]) * uint32_t(p.k) * uint32_t(p.nb);
+                cs->bcast[3] = !aborted(w) && wait_geq(&me->ret_done, need, w, SITE_EP_RETURNED);
+            }
+            __syncthreads();
+            stamp(p, 8);
+            if (cs->bcast[3]) combine_tokens(p, p.ep_t0[rank] + b, p.ep_t0[rank + 1], cpr);
+            stamp(p, 9);
+        }
+    }
+    cta_teardown<0>(p, cs, true);
 }
 
 // Unfused baseline, launch 1: routing per chunk.
@@ -1505,7 +1790,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_gather_kernel(const Params p) 
 
 // Unfused baseline, launch 5 (with a combine): tokens over the grid.
 __global__ void __launch_bounds__(NTHREADS, 1) mk_combine_kernel(const Params p) {
-    combine_tokens(p, blockIdx.x, gridDim.x);
+    combine_tokens(p, blockIdx.x, p.T, gridDim.x);
 }
 
 // Unfused baseline, launch 4: persistent expert GEMM over all tiles.
@@ -1526,7 +1811,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     build_tables(p, cs);
     __syncthreads();
     if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, false, flag, w);
-    else compute_role(p, &tmA, &tmB, &tmB3, cs, false, flag, w);
+    else compute_role(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), false, flag, w);
     cta_teardown<PAIR>(p, cs, true);
 }
 
@@ -1566,6 +1851,22 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
     if ((err = cudaOccupancyMaxActiveClusters(&clusters, mk_fused_kernel<1>, &cfg)) != cudaSuccess) return err;
     if (2 * clusters < grid) return cudaErrorCooperativeLaunchTooLarge;
     return cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3);
+}
+
+cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& b, int grid, cudaStream_t st) {
+    EpMaps maps{};
+    for (int r = 0; r < p.ranks; ++r) maps.a[r] = a[r];
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mk_ep_kernel, p, maps, b);
 }
 
 cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
@@ -1613,6 +1914,8 @@ cudaError_t set_kernel_attributes() {
     if ((err = cudaFuncSetAttribute(mk_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
         return err;
     if ((err = cudaFuncSetAttribute(mk_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
+        return err;
+    if ((err = cudaFuncSetAttribute(mk_ep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)))
         return err;
     return cudaFuncSetAttribute(mk_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
 }

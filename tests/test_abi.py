@@ -86,3 +86,21 @@ def test_workspace_size(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(mk.MkLibraryMissing):
         mk.lib(str(tmp_path / "nope.so"))
+
+
+def test_ep_workspace_size(lib):
+    T, H, F, E, k = 4096, 4096, 14336, 8, 2
+    for R in (1, 2, 4, 8):
+        n = mk.mk_ep_workspace_size(T, H, F, E, k, R)
+        # each rank can receive T * min(k, E/R) rows of H bf16 values
+        assert n >= R * T * min(k, E // R) * H * 2
+    assert mk.mk_ep_workspace_size(T, H, F, E, k, 3) == 0   # E not divisible by the ranks
+    assert mk.mk_ep_workspace_size(T, H, F, E, k, 0) == 0
+    assert mk.mk_ep_workspace_size(T, H, F, 16, k, 16) == 0  # more than 8 ranks
+    assert mk.mk_ep_workspace_size(T, 4000, F, E, k, 2) == 0
+
+
+def test_ep_argument_validation_is_synchronous(lib):
+    # ranks must divide E and lie in 1..8; checked before any device work
+    for R in (0, 3, 9):
+        assert mk.mk_moe_ep_sim(16, 16, 64, 512, 8, 2, 16, 1024, R, 16, 16, 16, 16, 16, 1) == mk.MK_ERR_INVALID_ARG

@@ -451,6 +451,31 @@ def run_ours(args, w):
             "vs_staged": ms_mean / dgms,
             "workspace_bytes": mk.mk_workspace_size(w.T, w.H, w.F, w.E, w.k, dgcfg),
             "staged_workspace_bytes": mk.mk_workspace_size(w.T, w.H, w.F, w.E, w.k, cfg)}
+        # expert parallelism simulated on this GPU: the most ranks (<= 8) that divide E
+        ranks = max(r for r in (1, 2, 4, 8) if w.E % r == 0)
+        ep_once = lambda c: mk.mk_moe_ep_sim(x, logits, w.T, w.H, w.E, w.k, W, w.F, ranks, out["y_sorted"],  # noqa: E731
+                                             out["src_index"], out["expert_offsets"], out["gate_w"], combined,
+                                             stream, c)
+        for _ in range(3):
+            flush.fill_(1)
+            if ep_once(cfg) != mk.MK_OK:
+                raise RuntimeError("mk_moe_ep_sim refused the configuration")
+        ep_evs = []
+        for _ in range(min(args.steps, 50)):
+            flush.fill_(1)
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            ep_once(cfg)
+            b_ev.record(stream)
+            ep_evs.append((a_ev, b_ev))
+        torch.cuda.synchronize()
+        if mk.mk_get_status(stream) != mk.MK_OK:
+            raise RuntimeError("expert-parallel path: device error")
+        ems = statistics.mean(a.elapsed_time(b) for a, b in ep_evs)
+        line["ep_sim"] = {"ranks": ranks, "ms": ems, "tflops": w.flop / (ems / 1e3) / 1e12,
+                          "vs_single_device_with_combine": cms / ems,
+                          "workspace_bytes": mk.mk_ep_workspace_size(w.T, w.H, w.F, w.E, w.k, ranks)}
+        mk.mk_release_workspace()
         # end to end through the host-buffer entry point
         xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
         lh = torch.from_numpy(l_np).pin_memory()

@@ -1134,40 +1134,68 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
 // out[t,:] = sum_j gate[t,j] * y[row of (t,j), :], fp32 in slot order
 // (deterministic, no atomics), stored in y's dtype.  y is y_sorted (row of
 // (t, j) from row_of) or, expert parallel, the token-major return rows (row
-// t*k + j).  Tokens t_first, t_first + stride, ... below t_end.  The pass is
-// HBM-bound, so each thread first issues 16 independent 16-byte loads (16/K
-// column vectors of the token's K rows) and only then accumulates and stores.
+// t*k + j).  Tokens t_first, t_first + stride, ... below t_end.
+//
+// The pass is bound by load latency: a token's K rows are only a few hundred
+// 16-byte vectors, fewer than the CTA's threads can keep in flight.  So the
+// CTA first stages the row indices and gates of a batch of its tokens in
+// shared memory and then treats the batch's (token, vector) pairs as one flat
+// range: every thread issues 16 independent 16-byte loads (U = 16/K vectors
+// of K rows, from any tokens) before it accumulates and stores.
+constexpr int COMBINE_BATCH = 256;  // tokens whose metadata is staged at once
+constexpr int COMBINE_SMEM = COMBINE_BATCH * MAX_K * 8;
+static_assert(COMBINE_SMEM <= SM_STAGE_END, "combine metadata must fit in the (idle) stage area");
+
 template <int K>
 __device__ void combine_tokens_k(const Params& p, int t_first, int t_end, int stride) {
     constexpr int U = 16 / K;  // 16-byte vectors per thread per pass
     const int F = p.F;
     const bool f32 = p.out_f32 != 0;
     const int nvec = f32 ? F / 4 : F / 8;
-    for (int t = t_first; t < t_end; t += stride) {
-        const uint4* src[K];
-        float g[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
+    const int ntok = t_first < t_end ? (t_end - t_first + stride - 1) / stride : 0;
+    int* srow = reinterpret_cast<int*>(smem_base());                 // [batch][K] row of (t, j)
+    float* sg = reinterpret_cast<float*>(smem_base() + COMBINE_BATCH * MAX_K * 4);  // [batch][K] gate
+    for (int i0 = 0; i0 < ntok; i0 += COMBINE_BATCH) {
+        const int nb = min(COMBINE_BATCH, ntok - i0);
+        __syncthreads();  // the previous batch's metadata is no longer read
+        for (int q = threadIdx.x; q < nb * K; q += NTHREADS) {
+            const int i = q / K, j = q - (q / K) * K;
+            const size_t tj = size_t(t_first + (i0 + i) * stride) * K + j;
             // in range even if an error path left a row unrecorded
-            const int r = p.ep ? t * K + j : min(max(__ldcg(p.row_of + size_t(t) * K + j), 0), p.rows - 1);
-            src[j] = f32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(p.y) + size_t(r) * F)
-                         : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.y) + size_t(r) * F);
-            g[j] = __ldcg(p.topk_gate + size_t(t) * K + j);
+            srow[q] = p.ep ? int(tj) : min(max(__ldcg(p.row_of + tj), 0), p.rows - 1);
+            sg[q] = __ldcg(p.topk_gate + tj);
         }
-        uint4* dst = f32 ? reinterpret_cast<uint4*>(static_cast<float*>(p.combine_out) + size_t(t) * F)
-                         : reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.combine_out) + size_t(t) * F);
-        for (int v0 = threadIdx.x; v0 < nvec; v0 += U * NTHREADS) {
+        __syncthreads();
+        const int units = nb * nvec;
+        // (token, vector) of this thread's first unit, advanced by steps of
+        // NTHREADS vectors instead of a division per unit
+        int tk = threadIdx.x / nvec, vc = threadIdx.x - (threadIdx.x / nvec) * nvec;
+        for (int f0 = threadIdx.x; f0 < units; f0 += U * NTHREADS) {
             uint4 buf[U][K];
+            int tok[U], vec[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * NTHREADS;
+                const int f = f0 + u * NTHREADS;
+                tok[u] = f < units ? tk : 0;
+                vec[u] = vc;
+                vc += NTHREADS;
+                while (vc >= nvec) {
+                    vc -= nvec;
+                    ++tk;
+                }
 #pragma unroll
-                for (int j = 0; j < K; ++j) buf[u][j] = v < nvec ? __ldcg(src[j] + v) : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < K; ++j) {
+                    const size_t off = size_t(srow[tok[u] * K + j]) * F;
+                    const uint4* src = f32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(p.y) + off)
+                                           : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.y) + off);
+                    buf[u][j] = f < units ? __ldcg(src + vec[u]) : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * NTHREADS;
-                if (v >= nvec) break;
+                if (f0 + u * NTHREADS >= units) break;
+                const float* g = sg + tok[u] * K;
+                const size_t t = size_t(t_first + (i0 + tok[u]) * stride);
                 if (f32) {
                     float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1177,8 +1205,9 @@ __device__ void combine_tokens_k(const Params& p, int t_first, int t_end, int st
                         a[2] += g[j] * __uint_as_float(buf[u][j].z);
                         a[3] += g[j] * __uint_as_float(buf[u][j].w);
                     }
-                    dst[v] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
-                                        __float_as_uint(a[3]));
+                    reinterpret_cast<uint4*>(static_cast<float*>(p.combine_out) + t * F)[vec[u]] =
+                        make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                   __float_as_uint(a[3]));
                 } else {
                     float a[8];
 #pragma unroll
@@ -1188,9 +1217,9 @@ __device__ void combine_tokens_k(const Params& p, int t_first, int t_end, int st
                         const uint32_t w4[4] = {buf[u][j].x, buf[u][j].y, buf[u][j].z, buf[u][j].w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
-                            a[2 * q] += g[j] * f.x;
-                            a[2 * q + 1] += g[j] * f.y;
+                            const float2 fv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
+                            a[2 * q] += g[j] * fv.x;
+                            a[2 * q + 1] += g[j] * fv.y;
                         }
                     }
                     uint32_t pk[4];
@@ -1199,7 +1228,8 @@ __device__ void combine_tokens_k(const Params& p, int t_first, int t_end, int st
                         const __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * q], a[2 * q + 1]);
                         pk[q] = *reinterpret_cast<const uint32_t*>(&h);
                     }
-                    dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.combine_out) + t * F)[vec[u]] =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
         }
@@ -1881,7 +1911,7 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     if (!p.pair) {
         mk_gemm_kernel<0><<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b, b3);
         if ((err = cudaGetLastError()) != cudaSuccess || !p.combine_out) return err;
-        mk_combine_kernel<<<grid, NTHREADS, 0, st>>>(p);
+        mk_combine_kernel<<<grid, NTHREADS, COMBINE_SMEM + 1024, st>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg{};
@@ -1897,7 +1927,7 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if ((err = cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b, b3)) != cudaSuccess || !p.combine_out) return err;
-    mk_combine_kernel<<<grid, NTHREADS, 0, st>>>(p);
+    mk_combine_kernel<<<grid, NTHREADS, COMBINE_SMEM + 1024, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -120,6 +120,8 @@ enum Site : int {
     SITE_EP_COUNTS = 15,
     SITE_EP_SCATTERED = 16,
     SITE_EP_RETURNED = 17,
+    SITE_PAIR_ALIGN = 18,
+    SITE_PAIR_CLUSTER = 19,
 };
 
 enum ErrCode : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_FAULT = 2 };

@@ -1289,6 +1289,16 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
     uint8_t* s = smem_base();
     const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
     const int total_items = cs->item_start[p.E];
+    // Self-check: the swizzled stages need a 1024-byte aligned base, the work
+    // records sent to the peer 16-byte slots.  A miss is recorded and the
+    // role is skipped (the call then times out) instead of faulting.
+    if ((smem_u32(s) & 1023u) != 0u || (mapa_shared(smem_u32(&cs->info[0]), 1) & 15u) != 0u) {
+        if (threadIdx.x == 0) {
+            record_error(ERR_FAULT, SITE_PAIR_ALIGN, smem_u32(s));
+            raise_abort(w);
+        }
+        return;
+    }
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1314,7 +1324,14 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
                         decode_item(p, cs, item, inf, gtile);
                     }
                     cs->info[slot] = inf;
-                    st_cluster_v4(mapa_shared(smem_u32(&cs->info[slot]), 1), inf.e, inf.row0, inf.nrows, inf.nbk);
+                    const uint32_t peer_info = mapa_shared(smem_u32(&cs->info[slot]), 1);
+                    if (peer_info & 15u) {  // self-check: a 16-byte store needs a 16-byte slot
+                        record_error(ERR_FAULT, SITE_PAIR_ALIGN, peer_info);
+                        raise_abort(w);
+                        ok = false;
+                        break;
+                    }
+                    st_cluster_v4(peer_info, inf.e, inf.row0, inf.nrows, inf.nbk);
                     mbar_arrive(&cs->info_full[slot]);
                     mbar_arrive_cluster(mapa_shared(smem_u32(&cs->info_full[slot]), 1));
                 } else {
@@ -1517,6 +1534,8 @@ __device__ void cta_setup(CtrlSmem* cs, bool with_tmem, bool direct) {
     tc_fence_after();
 }
 
+__device__ void cta_exit(const Params& p);
+
 template <int PAIR>
 __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
     tc_fence_before();
@@ -1528,6 +1547,12 @@ __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
         else tmem_dealloc(cs->tmem_base, TMEM_COLS);
     }
     if (PAIR) cluster_sync();  // neither CTA leaves while the other may touch its shared memory
+    cta_exit(p);
+}
+
+// Exit bookkeeping of every CTA; the last one out leaves the control blocks
+// ready for the next call.
+__device__ void cta_exit(const Params& p) {
     if (threadIdx.x == 0) {
         if (p.trace) p.trace_buf[blockIdx.x * TRACE_SLOTS + 15] = globaltimer();
         const uint32_t old = atom_add_acq_rel_u32(&p.ctl->exit_count, 1u);
@@ -1561,6 +1586,21 @@ __device__ void cta_teardown(const Params& p, CtrlSmem* cs, bool with_tmem) {
 
 // ------------------------------------------------------------- kernels -----
 
+// Self-check of the SM-pair kernels: every pair-specific step (peer shared
+// memory, pair TMEM allocation, pair MMAs) assumes a cluster of exactly two
+// CTAs.  Launched any other way, the CTA records the fact and only does its
+// exit bookkeeping.
+__device__ bool in_cta_pair(const Params& p, const WaitCtx& w) {
+    const uint32_t n = cluster_nctarank();
+    if (n == 2u) return true;
+    if (threadIdx.x == 0) {
+        record_error(ERR_FAULT, SITE_PAIR_CLUSTER, n);
+        raise_abort(w);
+    }
+    cta_exit(p);
+    return false;
+}
+
 template <int PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mk_fused_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -1574,6 +1614,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    if (PAIR && !in_cta_pair(p, w)) return;
     cta_setup<PAIR>(cs, p.compute != 0, p.direct != 0);
 
     // This call's readiness flags start at 0.  Cleared before the routing
@@ -1835,6 +1876,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    if (PAIR && !in_cta_pair(p, w)) return;
     cta_setup<PAIR>(cs, true, p.direct != 0);
     for (int e = threadIdx.x; e < p.E; e += NTHREADS) cs->tot[e] = p.expert_offsets[e + 1] - p.expert_offsets[e];
     __syncthreads();

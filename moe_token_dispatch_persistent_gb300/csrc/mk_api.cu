@@ -50,6 +50,7 @@ struct DevInfo {
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuStreamWaitValue32_v11070 g_wait_value = nullptr;
 thread_local mk_launch_info_t g_last_info{};
 uint32_t g_last_err[4] = {0, 0, 0, 0};
 
@@ -63,6 +64,12 @@ std::map<std::pair<int, cudaStream_t>, WsEntry> g_ws_ep;  // expert-parallel lay
 struct HostStage {
     void* ptr = nullptr;
     size_t bytes = 0;
+    cudaStream_t copy = nullptr;     // streams finished result chunks to the host
+    cudaEvent_t copied = nullptr;    // recorded on `copy` after the last chunk
+    cudaEvent_t computed = nullptr;  // recorded on the caller's stream after the kernel (fallback)
+    uint32_t* flags = nullptr;       // chunk flags: plain device memory (the driver's stream waits
+                                     // do not accept stream-ordered pool memory)
+    uint32_t seq = 0;                // calls made with this stage (chunk flags hold it)
 };
 std::map<std::pair<int, cudaStream_t>, HostStage> g_host_stage;
 
@@ -96,6 +103,14 @@ mk_status_t device_info(int* dev_out, DevInfo** info) {
                 q != cudaDriverEntryPointSuccess || fn == nullptr)
                 return MK_ERR_CUDA;
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            // stream waits on a value in memory (optional: without them the host
+            // entry point copies the results after the kernel instead)
+            void* wf = nullptr;
+            cudaDriverEntryPointQueryResult wq{};
+            if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &wf, 11070, cudaEnableDefault, &wq) ==
+                    cudaSuccess &&
+                wq == cudaDriverEntryPointSuccess)
+                g_wait_value = reinterpret_cast<PFN_cuStreamWaitValue32_v11070>(wf);
         }
         d.ready = true;
     }
@@ -246,11 +261,23 @@ size_t mk_workspace_size(int T, int H, int F, int E, int k, const mk_config_t* c
 
 namespace {
 
+// Streamed results: chunk counters and flags in device memory, rows per
+// chunk, and this call's sequence number (see Params::stream_done).
+struct StreamOut {
+    uint32_t* done;
+    uint32_t* flag;
+    int rows;
+    uint32_t seq;
+};
+
 // The whole path; with combine_out it also combines each token's expert
-// rows (gated sum) into combine_out[T,F].
+// rows (gated sum) into combine_out[T,F].  With `so` (fused single-SM path
+// only, else MK_ERR_UNSUPPORTED) the kernel also raises each result chunk's
+// flag as it completes.
 mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, int k, const void* W, const void* W3,
                      int F, void* y_sorted, int32_t* src_index, int32_t* expert_offsets, float* gate_w,
-                     void* combine_out, void* stream, const mk_config_t* cfg_in, void* workspace, size_t ws_bytes) {
+                     void* combine_out, void* stream, const mk_config_t* cfg_in, void* workspace, size_t ws_bytes,
+                     const StreamOut* so = nullptr) {
     g_last_info = mk_launch_info_t{};
     mk_status_t s = validate_sizes(T, H, E, k, F);
     if (s != MK_OK) return s;
@@ -368,6 +395,13 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.ranks = 1;  // routing chunks over [0, T)
     p.ep_t0[1] = T;
     p.ep_c0[1] = nch;
+    if (so) {
+        if (c.mode != MK_MODE_FUSED || pair || so->rows < 1) return MK_ERR_UNSUPPORTED;
+        p.stream_done = so->done;
+        p.stream_flag = so->flag;
+        p.stream_rows = so->rows;
+        p.stream_seq = so->seq;
+    }
 
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof(tmA));
@@ -606,11 +640,25 @@ mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_ho
     if ((s = device_info(&dev, &d)) != MK_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t rows = size_t(T) * k;
-    const size_t ybytes = rows * F * (c.out_dtype == MK_OUT_F32 ? 4 : 2);
+    const size_t row_bytes = size_t(F) * (c.out_dtype == MK_OUT_F32 ? 4 : 2);
+    const size_t ybytes = rows * row_bytes;
+    // The results go back in chunks of sorted rows as the kernel completes
+    // them, on a second stream, so the copy overlaps the GEMM (the host link,
+    // not the GPU, bounds this call).  The fused single-SM path raises the
+    // chunk flags; other configurations copy after the kernel.
+    const bool streamed = T > 0 && g_wait_value && c.mode == MK_MODE_FUSED && c.mma_pair != MK_MMA_PAIR;
+    if (!streamed && getenv("MK_LOG"))
+        fprintf(stderr, "[mk] host entry: results copied after the kernel (stream waits %s)\n",
+                g_wait_value ? "available" : "unavailable");
+    constexpr int kMaxChunks = 64;
+    const size_t per = (rows + kMaxChunks - 1) / kMaxChunks;
+    const int srows = int(per > 512 ? per : 512);
+    const int nchunks = int((rows + srows - 1) / srows);  // <= kMaxChunks
     const size_t o_x = 0, o_l = ws_align(o_x + size_t(T) * H * 2), o_y = ws_align(o_l + size_t(T) * E * 4),
                  o_s = ws_align(o_y + ybytes), o_o = ws_align(o_s + rows * 4), o_g = ws_align(o_o + size_t(E + 1) * 4),
-                 total = ws_align(o_g + rows * 4);
+                 o_done = ws_align(o_g + rows * 4), total = ws_align(o_done + size_t(nchunks) * 4);
     uint8_t* base = nullptr;
+    HostStage* hs = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         HostStage& h = g_host_stage[{dev, st}];
@@ -620,22 +668,62 @@ mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_ho
             h.bytes = 0;
             if (cudaMallocAsync(&h.ptr, total, st) != cudaSuccess) return MK_ERR_CUDA;
             h.bytes = total;
+
+        }
+        if (streamed && !h.copy) {
+            if (cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h.copied, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h.computed, cudaEventDisableTiming) != cudaSuccess ||
+                cudaMalloc(&h.flags, kMaxChunks * sizeof(uint32_t)) != cudaSuccess ||
+                cudaMemset(h.flags, 0, kMaxChunks * sizeof(uint32_t)) != cudaSuccess)  // below every sequence number
+                return MK_ERR_CUDA;
         }
         base = static_cast<uint8_t*>(h.ptr);
+        hs = &h;
     }
     if (T > 0) {
         if (cudaMemcpyAsync(base + o_x, x_host, size_t(T) * H * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
             cudaMemcpyAsync(base + o_l, logits_host, size_t(T) * E * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
             return MK_ERR_CUDA;
     }
-    s = mk_moe_dispatch_gemm_ex(base + o_x, reinterpret_cast<const float*>(base + o_l), T, H, E, k, W, F, base + o_y,
-                                reinterpret_cast<int32_t*>(base + o_s), reinterpret_cast<int32_t*>(base + o_o),
-                                reinterpret_cast<float*>(base + o_g), stream, &c, nullptr, 0);
+    StreamOut so{reinterpret_cast<uint32_t*>(base + o_done), hs->flags, srows, 0u};
+    if (streamed) so.seq = ++hs->seq;
+    s = run_path(base + o_x, reinterpret_cast<const float*>(base + o_l), T, H, E, k, W, nullptr, F, base + o_y,
+                 reinterpret_cast<int32_t*>(base + o_s), reinterpret_cast<int32_t*>(base + o_o),
+                 reinterpret_cast<float*>(base + o_g), nullptr, stream, &c, nullptr, 0, streamed ? &so : nullptr);
     if (s != MK_OK) return s;
+    if (streamed) {
+        // chunk i is copied once the kernel has raised its flag to this call's
+        // number (the last CTA out raises every flag, even if the call gave up).
+        // If the driver refuses a wait, the remaining chunks wait for the whole
+        // kernel instead.
+        bool waits = true;
+        int wait_err = 0;
+        for (int i = 0; i < nchunks; ++i) {
+            const size_t r0 = size_t(i) * srows, nr = (r0 + srows <= rows ? size_t(srows) : rows - r0);
+            CUresult wr = CUDA_SUCCESS;
+            if (waits && (wr = g_wait_value(hs->copy, reinterpret_cast<CUdeviceptr>(so.flag + i), so.seq,
+                                            CU_STREAM_WAIT_VALUE_GEQ)) != CUDA_SUCCESS) {
+                waits = false;
+                wait_err = int(wr);
+                if (cudaEventRecord(hs->computed, st) != cudaSuccess ||
+                    cudaStreamWaitEvent(hs->copy, hs->computed, 0) != cudaSuccess)
+                    return MK_ERR_CUDA;
+            }
+            if (cudaMemcpyAsync(static_cast<uint8_t*>(y_sorted_host) + r0 * row_bytes, base + o_y + r0 * row_bytes,
+                                nr * row_bytes, cudaMemcpyDeviceToHost, hs->copy) != cudaSuccess)
+                return MK_ERR_CUDA;
+        }
+        if (cudaEventRecord(hs->copied, hs->copy) != cudaSuccess || cudaStreamWaitEvent(st, hs->copied, 0) != cudaSuccess)
+            return MK_ERR_CUDA;
+        if (getenv("MK_LOG"))
+            fprintf(stderr, "[mk] host entry: %d result chunks of %d rows streamed, stream waits %s (%d)\n", nchunks,
+                    srows, waits ? "used" : "refused, copies follow the kernel", wait_err);
+    }
     if (cudaMemcpyAsync(expert_offsets_host, base + o_o, size_t(E + 1) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MK_ERR_CUDA;
     if (T > 0) {
-        if (cudaMemcpyAsync(y_sorted_host, base + o_y, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        if ((!streamed && cudaMemcpyAsync(y_sorted_host, base + o_y, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
             cudaMemcpyAsync(src_index_host, base + o_s, rows * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
             cudaMemcpyAsync(gate_w_host, base + o_g, rows * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
             return MK_ERR_CUDA;
@@ -707,10 +795,13 @@ void mk_release_workspace(void) {
     }
     g_ws_ep.clear();
     for (auto& kv : g_host_stage) {
-        if (!kv.second.ptr) continue;
         cudaSetDevice(kv.first.first);
         cudaDeviceSynchronize();
-        cudaFree(kv.second.ptr);
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+        if (kv.second.copy) cudaStreamDestroy(kv.second.copy);
+        if (kv.second.copied) cudaEventDestroy(kv.second.copied);
+        if (kv.second.computed) cudaEventDestroy(kv.second.computed);
+        if (kv.second.flags) cudaFree(kv.second.flags);
     }
     g_host_stage.clear();
     cudaSetDevice(cur);

@@ -169,6 +169,14 @@ struct Params {
     uint16_t* xs;            // [T*k,H] bf16 staging
     unsigned long long* trace_buf;  // [grid][TRACE_SLOTS]
     int max_tiles;
+    // Streamed results (host-buffer entry point, fused single-SM path): sorted
+    // rows [c*stream_rows, (c+1)*stream_rows) form chunk c.  Once every row of
+    // the chunk is stored for every N-block, stream_flag[c] = stream_seq, and a
+    // copy stream waiting on that value starts copying the chunk to the host.
+    uint32_t* stream_done;   // [chunks] (row, N-block) results stored; cleared per call (null: off)
+    uint32_t* stream_flag;   // [chunks] sequence number of the call that completed the chunk
+    int stream_rows;
+    uint32_t stream_seq;
     // token ranges of the routing chunks: rank r's tokens [ep_t0[r], ep_t0[r+1])
     // are split into the chunks [ep_c0[r], ep_c0[r+1]) (one rank, [0, T), when
     // not simulating expert parallelism)

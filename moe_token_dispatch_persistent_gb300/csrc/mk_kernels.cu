@@ -1121,6 +1121,23 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 if (src >= 0 && lane == __ffs(peers) - 1)
                     atom_add_acq_rel_u32(&p.ep_ctl[src]->ret_done, uint32_t(__popc(peers)));
             }
+            if (p.stream_done) {
+                // streamed results: count this item's stored rows per chunk; the
+                // warp that completes a chunk raises its flag for the copy stream
+                const int c = rowok ? int(row / uint32_t(p.stream_rows)) : -1;
+                __threadfence();  // this lane's stores before the count that publishes them
+                __syncwarp();
+                const uint32_t peers = __match_any_sync(0xffffffffu, c);
+                if (c >= 0 && lane == __ffs(peers) - 1) {
+                    const uint32_t n = uint32_t(__popc(peers));
+                    const uint32_t target =
+                        uint32_t(min(p.rows - c * p.stream_rows, p.stream_rows)) * uint32_t(p.nb);
+                    if (atom_add_acq_rel_u32(&p.stream_done[c], n) + n == target) {
+                        __threadfence_system();
+                        st_release_sys_u32(&p.stream_flag[c], p.stream_seq);
+                    }
+                }
+            }
             tc_fence_before();
             mbar_arrive(&cs->acc_empty[acc]);
             acc ^= 1u;
@@ -1567,6 +1584,13 @@ __device__ void cta_exit(const Params& p) {
             c->bar_computed = 0;
             c->abort = 0;
             c->epoch = c->epoch + 1u;  // calls completed on this workspace
+            if (p.stream_flag) {
+                // a call that gave up still releases every chunk: the copy
+                // stream never waits past the end of the call
+                __threadfence_system();
+                const int nchunks = (p.rows + p.stream_rows - 1) / p.stream_rows;
+                for (int i = 0; i < nchunks; ++i) st_release_sys_u32(&p.stream_flag[i], p.stream_seq);
+            }
             if (p.ep) {
                 for (int r = 0; r < p.ranks; ++r) {
                     EpCtl* q = p.ep_ctl[r];
@@ -1620,6 +1644,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // This call's readiness flags start at 0.  Cleared before the routing
     // barrier; they are set only after it, so no stale value is ever seen.
     for (int i = blockIdx.x * NTHREADS + threadIdx.x; i < p.max_tiles; i += gridDim.x * NTHREADS) p.ready[i] = 0u;
+    if (p.stream_done) {
+        const int nchunks = (p.rows + p.stream_rows - 1) / p.stream_rows;
+        for (int i = blockIdx.x * NTHREADS + threadIdx.x; i < nchunks; i += gridDim.x * NTHREADS) p.stream_done[i] = 0u;
+    }
 
     // phase R
     for (int c = blockIdx.x; c < p.nch; c += gridDim.x) route_chunk(p, c);

@@ -84,6 +84,13 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
     return v;
 }
 
+// Release store at system scope: visible to observers outside the SMs
+// (a stream waiting on the value) after every write this thread ordered
+// before it.
+__device__ __forceinline__ void st_release_sys_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

@@ -216,7 +216,13 @@ size_t mk_ep_workspace_size(int T, int H, int F, int E, int k, int ranks);
  * (pinned memory gives asynchronous copies); W stays on the device (expert
  * weights are resident).  Copies the inputs in, runs the fused path, copies
  * the outputs back, and synchronises `stream` before returning, so the host
- * buffers are ready on return.  Device staging comes from the library cache. */
+ * buffers are ready on return.  With the fused single-SM path, y_sorted goes
+ * back in chunks of sorted rows (at most 64) while the kernel still runs: the
+ * kernel raises a flag per finished chunk and a second, library-owned stream
+ * waits on it and copies the chunk; other configurations copy after the
+ * kernel.  Device staging comes from the library cache.  The library's
+ * stream and chunk flags belong to (device, stream); calls on one stream run
+ * one after another. */
 mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_host, int T, int H, int E,
                                       int k, const void* W, int F, void* y_sorted_host,
                                       int32_t* src_index_host, int32_t* expert_offsets_host,

@@ -347,6 +347,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.E = E;
     p.k = k;
     p.out_f32 = c.out_dtype == MK_OUT_F32;
+    p.y_v8 = aligned(y_sorted, 32) ? 1 : 0;
     p.rows = rows;
     p.nch = nch;
     p.gated = W3 ? 1 : 0;
@@ -512,6 +513,7 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     p.E = E;
     p.k = k;
     p.out_f32 = c.out_dtype == MK_OUT_F32;
+    p.y_v8 = aligned(y_tok, 32) ? 1 : 0;
     p.rows = T * k;
     p.nch = L.nch;
     p.nb = nb;

@@ -138,6 +138,7 @@ struct Params {
     float* gate_w;           // [T*k]
     int T, H, F, E, k;
     int out_f32;
+    int y_v8;                // y is 32-byte aligned: results go out as 256-bit stores
     // derived sizes
     int rows;                // T*k
     int nch;                 // routing chunks

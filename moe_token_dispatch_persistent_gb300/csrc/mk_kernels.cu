@@ -697,29 +697,44 @@ __device__ __forceinline__ void decode_item(const Params& p, const CtrlSmem* cs,
 }
 
 constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
-// Gated FFN: two N = 128 products (gate W1, up W3) per item share the A tile.
+// Gated FFN: 128 output columns per item; the item's B stage holds those
+// columns of both projections (gate W1, up W3) side by side.
 constexpr int GATED_BN = BN / 2;
-constexpr uint32_t IDESC_GATED = umma_idesc_bf16(BM, GATED_BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+static_assert(B_STAGE_BYTES / 2 == (GATED_BN / 64) * B_CHUNK_BYTES, "W3 chunks follow the W1 chunks directly");
 
 // One thread's 32 consecutive fp32 results of row `row`, columns [col, col+32),
-// stored as bf16 (round to nearest even) or f32.
+// stored as bf16 (round to nearest even) or f32.  Each lane writes its own
+// row, so a warp instruction touches 32 rows: with a 32-byte aligned y every
+// store fills whole 32-byte sectors (256-bit stores; a 16-byte store writes
+// half a sector, and the epilogue then costs about 6% of the kernel).
 __device__ __forceinline__ void store_row32(const Params& p, size_t row, int col, const uint32_t (&r)[32]) {
     if (p.out_f32) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.y) + row * p.F + col);
+        float* dst = static_cast<float*>(p.y) + row * p.F + col;
+        if (p.y_v8) {
 #pragma unroll
-        for (int v = 0; v < 8; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+            for (int v = 0; v < 4; ++v)
+                st_global_v8(dst + 8 * v, r[8 * v], r[8 * v + 1], r[8 * v + 2], r[8 * v + 3], r[8 * v + 4],
+                             r[8 * v + 5], r[8 * v + 6], r[8 * v + 7]);
+        } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) d4[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        }
     } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + row * p.F + col);
+        uint32_t pk[16];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            uint32_t pk[4];
+        for (int u = 0; u < 16; ++u) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+            pk[u] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        uint16_t* dst = static_cast<uint16_t*>(p.y) + row * p.F + col;
+        if (p.y_v8) {
+            st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+            st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+        } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const __nv_bfloat162 h =
-                    __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * u]), __uint_as_float(r[8 * v + 2 * u + 1]));
-                pk[u] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
     }
 }
@@ -1030,17 +1045,12 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                         const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
                         // B: N-major, 128B swizzle; 64-column chunks 8 KiB apart (LBO),
                         // 8-row K groups 1024 B apart (SBO); +2 KiB per K=16
-                        if (p.gated) {
-                            // gate and up projections side by side in the accumulator:
-                            // columns [0, 128) = A.W1, [128, 256) = A.W3
-                            const uint64_t b1 = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
-                            const uint64_t b3 = umma_desc_sw128(b0 + B_STAGE_BYTES / 2 + kk * 2048, B_CHUNK_BYTES, 1024);
-                            tc_mma_f16(d, ad, b1, IDESC_GATED, (kb | kk) != 0 ? 1u : 0u);
-                            tc_mma_f16(d + GATED_BN, ad, b3, IDESC_GATED, (kb | kk) != 0 ? 1u : 0u);
-                        } else {
-                            const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
-                            tc_mma_f16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                        }
+                        // Gated: the stage holds 128 columns of W1 then the same 128
+                        // of W3 as four consecutive 64-column chunks, so one N = 256
+                        // product leaves A.W1 in accumulator columns [0, 128) and
+                        // A.W3 in [128, 256).
+                        const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
+                        tc_mma_f16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued = true;
                     tc_commit(&cs->empty[stage]);
@@ -1478,27 +1488,7 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + cc * 32, r);
                 tmem_ld_wait();
-                if (rowok) {
-                    if (p.out_f32) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.y) + row * p.F + col);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + row * p.F + col);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * u]),
-                                                                               __uint_as_float(r[8 * v + 2 * u + 1]));
-                                pk[u] = *reinterpret_cast<const uint32_t*>(&h);
-                            }
-                            dst[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
-                    }
-                }
+                if (rowok) store_row32(p, row, col, r);
             }
             tc_fence_before();
             __syncwarp();

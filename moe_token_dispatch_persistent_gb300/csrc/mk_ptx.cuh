@@ -84,6 +84,14 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
     return v;
 }
 
+// One 256-bit global store (32-byte aligned address).
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 // Release store at system scope: visible to observers outside the SMs
 // (a stream waiting on the value) after every write this thread ordered
 // before it.

@@ -51,3 +51,22 @@ def test_malformed_lines_are_skipped():
     t0 = 1_800_000_000.0
     c = _sampler_with(["garbage\n", "[N/A], 0\n", _line(t0 + 0.5, 2070)], t0, t0 + 1.0).stop()
     assert c["samples"] == 1 and c["sm_mhz"] == 2070
+
+
+def test_reference_arm_prints_one_json_line():
+    """`bench.py --impl reference` times the CPU oracle (no GPU needed) and
+    prints the contract's line with impl, cpu_baseline and e2e."""
+    import json
+
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "1",
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"].startswith("tiny")

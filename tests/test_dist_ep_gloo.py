@@ -129,12 +129,18 @@ def test_expert_parallel_exchange_matches_single_process(R, T, E, k):
     procs = [ctx.Process(target=_ep_worker, args=(r, R, port, q, T, H, F, E, k, seed)) for r in range(R)]
     for p in procs:
         p.start()
-    results = sorted((q.get(timeout=120) for _ in range(R)), key=lambda r: r[0])
-    for r in results:
+    results = []
+    for _ in range(R):
+        r = q.get(timeout=120)
         if len(r) == 3 and r[1] == "error":
+            # the other ranks may be blocked in a collective with the failed one
             for p in procs:
-                p.join(timeout=30)
+                p.join(timeout=5)
+                if p.is_alive():
+                    p.kill()
             pytest.fail(f"rank {r[0]} failed:\n{r[2]}")
+        results.append(r)
+    results.sort(key=lambda r: r[0])
     for p in procs:
         p.join(timeout=120)
         assert p.exitcode == 0

@@ -68,12 +68,27 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_code_digest(paths) -> str:
+    """sha256 of the sources' code: comments and whitespace removed, so an
+    edit of a comment does not invalidate a capture (nothing else changes
+    the compiled kernel)."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for src in paths:
+        with open(os.path.join(ROOT, src), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()
+
+
 def ncu_traffic(workload_name: str):
     """DRAM bytes (read + write) per launch of the fused kernel from the
     committed ncu capture of this workload, or None when there is none or the
-    kernel sources changed since it was taken."""
-    import hashlib
-
+    kernel code changed since it was taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             rec = json.load(f).get(workload_name)
@@ -81,14 +96,11 @@ def ncu_traffic(workload_name: str):
         return None
     if not rec:
         return None
-    h = hashlib.sha256()
     try:
-        for src in rec["kernel_sources"]:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                h.update(f.read())
+        digest = kernel_code_digest(rec["kernel_sources"])
     except OSError:
         return None
-    return rec["bytes_per_launch"] if h.hexdigest() == rec["kernel_sha256"] else None
+    return rec["bytes_per_launch"] if digest == rec["kernel_code_sha256"] else None
 
 
 def workload_config(w: synth.Workload, extra=None):

@@ -70,3 +70,14 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["value"] == d["value"] and d["e2e"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"].startswith("tiny")
+
+
+def test_kernel_code_digest_ignores_comments_only(tmp_path, monkeypatch):
+    a = tmp_path / "a.cu"
+    a.write_text("int f(int x) {  // doubles\n    return 2 * x; /* twice */\n}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d0 = bench.kernel_code_digest(["a.cu"])
+    a.write_text("// a header comment\nint f(int x) {\n  return 2 * x;   // still twice\n}\n")
+    assert bench.kernel_code_digest(["a.cu"]) == d0
+    a.write_text("int f(int x) {\n  return 3 * x;\n}\n")
+    assert bench.kernel_code_digest(["a.cu"]) != d0

@@ -224,3 +224,26 @@ def test_trace_records_phases():
     tr = mk.mk_read_trace(T, H, E, k, info["grid_ctas"])
     assert (tr[:, 0] > 0).all() and (tr[:, 15] >= tr[:, 0]).all()
     assert (tr[: info["dispatch_ctas"], 5] > 0).all()  # every dispatch CTA finished its gather
+
+
+def test_two_streams_at_once():
+    """Calls on two streams, enqueued back to back without synchronising:
+    each stream has its own cached workspace and both results are right."""
+    a_in = gu.to_device(*_inputs(1200, 256, 512, 8, 2, seed=51))
+    b_in = gu.to_device(*_inputs(700, 256, 384, 16, 4, seed=52))
+    ref_a = gu.run_gpu(*a_in, 2)
+    ref_b = gu.run_gpu(*b_in, 4)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            oa = mk.moe_dispatch_gemm(*a_in, 2, stream=s1, check=False)
+        with torch.cuda.stream(s2):
+            ob = mk.moe_dispatch_gemm(*b_in, 4, stream=s2, check=False)
+        outs.append((oa, ob))
+    assert mk.mk_get_status(s1) == mk.MK_OK and mk.mk_get_status(s2) == mk.MK_OK
+    for oa, ob in outs:
+        assert np.array_equal(oa["y_sorted"].float().cpu().numpy(), ref_a["y"])
+        assert np.array_equal(ob["y_sorted"].float().cpu().numpy(), ref_b["y"])
+        assert np.array_equal(oa["src_index"].cpu().numpy(), ref_a["src_index"])
+        assert np.array_equal(ob["src_index"].cpu().numpy(), ref_b["src_index"])

@@ -209,6 +209,18 @@ mk_status_t mk_moe_ep_sim(const void* x, const float* logits, int T, int H, int 
                           int ranks, void* y_tok, int32_t* src_index, int32_t* expert_offsets, float* gate_w,
                           void* out, void* stream, const mk_config_t* cfg, void* workspace, size_t ws_bytes);
 
+/* The gated (SwiGLU) expert FFN of mk_moe_dispatch_gated under the same
+ * expert-parallel simulation: each rank computes
+ * h = silu(x[t].W1[e]) * (x[t].W3[e]) for the rows it received and returns
+ * them to the sending ranks (h_tok[t*k + j]); with `out`, each rank combines
+ * its own tokens' h rows.  W1, W3: [E,H,F] bf16, device, 16-byte aligned.
+ * Other arguments, outputs and errors as for mk_moe_ep_sim; the workspace
+ * is the same size. */
+mk_status_t mk_moe_ep_sim_gated(const void* x, const float* logits, int T, int H, int E, int k, const void* W1,
+                                const void* W3, int F, int ranks, void* h_tok, int32_t* src_index,
+                                int32_t* expert_offsets, float* gate_w, void* out, void* stream,
+                                const mk_config_t* cfg, void* workspace, size_t ws_bytes);
+
 /* Workspace bytes mk_moe_ep_sim needs (0 for invalid sizes). */
 size_t mk_ep_workspace_size(int T, int H, int F, int E, int k, int ranks);
 

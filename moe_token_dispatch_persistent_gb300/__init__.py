@@ -48,6 +48,7 @@ ABI_FUNCTIONS = (
     "mk_moe_dispatch_gemm_host",
     "mk_moe_dispatch_gemm_noalloc",
     "mk_moe_ep_sim",
+    "mk_moe_ep_sim_gated",
     "mk_ep_workspace_size",
     "mk_workspace_size",
     "mk_get_status",
@@ -133,6 +134,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     h.mk_moe_ep_sim.argtypes = [_p, _p, _i, _i, _i, _i, _p, _i, _i, _p, _p, _p, _p, _p, _p,
                                 ctypes.POINTER(mk_config_t), _p, ctypes.c_size_t]
     h.mk_moe_ep_sim.restype = _i
+    h.mk_moe_ep_sim_gated.argtypes = [_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p,
+                                      ctypes.POINTER(mk_config_t), _p, ctypes.c_size_t]
+    h.mk_moe_ep_sim_gated.restype = _i
     h.mk_ep_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
     h.mk_ep_workspace_size.restype = ctypes.c_size_t
     h.mk_workspace_size.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(mk_config_t)]
@@ -274,15 +278,25 @@ def mk_moe_ep_sim(x, logits, T, H, E, k, W, F, ranks, y_tok, src_index, expert_o
                                    ctypes.byref(cfg) if cfg is not None else None, _ptr(workspace), int(ws_bytes)))
 
 
+def mk_moe_ep_sim_gated(x, logits, T, H, E, k, W1, W3, F, ranks, h_tok, src_index, expert_offsets, gate_w,
+                        out=None, stream=None, cfg: mk_config_t | None = None, workspace=None, ws_bytes: int = 0) -> int:
+    return int(lib().mk_moe_ep_sim_gated(_ptr(x), _ptr(logits), T, H, E, k, _ptr(W1), _ptr(W3), F, ranks,
+                                         _ptr(h_tok), _ptr(src_index), _ptr(expert_offsets), _ptr(gate_w), _ptr(out),
+                                         _stream(stream), ctypes.byref(cfg) if cfg is not None else None,
+                                         _ptr(workspace), int(ws_bytes)))
+
+
 def mk_ep_workspace_size(T, H, F, E, k, ranks) -> int:
     return int(lib().mk_ep_workspace_size(T, H, F, E, k, ranks))
 
 
-def moe_ep_sim(x, logits, W, k, ranks, cfg: mk_config_t | None = None, stream=None, combine=True, check=True):
+def moe_ep_sim(x, logits, W, k, ranks, cfg: mk_config_t | None = None, stream=None, combine=True, check=True,
+               W3=None):
     """Expert parallelism over ``ranks`` logical ranks simulated on one GPU;
     returns ``y_tok[T*k,F]`` (token-major), the receive metadata
     (``src_index``, ``gate_w``, ``expert_offsets``) and, with ``combine``,
-    ``out[T,F]``."""
+    ``out[T,F]``.  With ``W3`` the experts are the gated (SwiGLU) FFN with
+    ``W`` as W1, and ``y_tok`` holds h."""
     import torch
 
     T, H = x.shape
@@ -290,8 +304,12 @@ def moe_ep_sim(x, logits, W, k, ranks, cfg: mk_config_t | None = None, stream=No
     o = alloc_outputs(T, F, E, k, cfg.out_dtype if cfg is not None else MK_OUT_BF16, x.device)
     o["y_tok"] = o.pop("y_sorted")
     o["out"] = torch.empty((T, F), dtype=o["y_tok"].dtype, device=x.device) if combine else None
-    st = mk_moe_ep_sim(x, logits, T, H, E, k, W, F, ranks, o["y_tok"], o["src_index"], o["expert_offsets"],
-                       o["gate_w"], o["out"], stream, cfg)
+    if W3 is None:
+        st = mk_moe_ep_sim(x, logits, T, H, E, k, W, F, ranks, o["y_tok"], o["src_index"], o["expert_offsets"],
+                           o["gate_w"], o["out"], stream, cfg)
+    else:
+        st = mk_moe_ep_sim_gated(x, logits, T, H, E, k, W, W3, F, ranks, o["y_tok"], o["src_index"],
+                                 o["expert_offsets"], o["gate_w"], o["out"], stream, cfg)
     _check(st, "mk_moe_ep_sim")
     if check:
         _check(mk_get_status(stream), "device status")

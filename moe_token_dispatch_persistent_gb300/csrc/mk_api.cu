@@ -27,7 +27,8 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
                          cudaStream_t st);
 cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                            int grid, cudaStream_t st);
-cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& b, int grid, cudaStream_t st);
+cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& b, const CUtensorMap& b3, int grid,
+                      cudaStream_t st);
 cudaError_t set_kernel_attributes();
 cudaError_t fused_max_blocks_per_sm(int* n);
 cudaError_t read_and_clear_error(uint32_t out[4], cudaStream_t st);
@@ -441,7 +442,8 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
 }
 
 // Expert parallelism simulated with `ranks` logical ranks in one launch.
-mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F, int ranks,
+mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int k, const void* W, const void* W3,
+                   int F, int ranks,
                    void* y_tok, int32_t* src_index, int32_t* expert_offsets, float* gate_w, void* out, void* stream,
                    const mk_config_t* cfg_in, void* workspace, size_t ws_bytes) {
     g_last_info = mk_launch_info_t{};
@@ -463,6 +465,7 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     if (!expert_offsets || !aligned(expert_offsets, 4)) return MK_ERR_INVALID_ARG;
     if (T > 0) {
         if (!x || !logits || !W || !y_tok || !src_index || !gate_w) return MK_ERR_INVALID_ARG;
+        if (W3 && !aligned(W3, 16)) return MK_ERR_INVALID_ARG;
         if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y_tok, 16) || !aligned(logits, 4) ||
             !aligned(src_index, 4) || !aligned(gate_w, 4))
             return MK_ERR_INVALID_ARG;
@@ -486,7 +489,7 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
         const int nt = ep_token0(T, ranks, r + 1) - ep_token0(T, ranks, r);
         if ((nt + ROUTE_CHUNK - 1) / ROUTE_CHUNK > cpr * MAX_CHUNKS_PER_CTA) return MK_ERR_UNSUPPORTED;
     }
-    const int bnw = BN;
+    const int bnw = W3 ? BN / 2 : BN;  // gated: 128 columns of each projection per item
     const int nb = (F + bnw - 1) / bnw;
     // completion counts: a rank's (row, N-block) results in 32 bits
     if (uint64_t(T) * uint64_t(k) * uint64_t(nb) >= (uint64_t(1) << 32)) return MK_ERR_UNSUPPORTED;
@@ -503,6 +506,8 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     p.x = static_cast<const uint16_t*>(x);
     p.logits = logits;
     p.W = static_cast<const uint16_t*>(W);
+    p.W3 = static_cast<const uint16_t*>(W3);
+    p.gated = W3 ? 1 : 0;
     p.y = y_tok;
     p.src_index = src_index;
     p.expert_offsets = expert_offsets;
@@ -566,8 +571,11 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     }
     if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
+    CUtensorMap tmB3 = tmB;
+    if (W3 && encode_2d(&tmB3, W3, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+        return MK_ERR_CUDA;
 
-    const cudaError_t err = launch_ep(p, tmA, tmB, grid, st);
+    const cudaError_t err = launch_ep(p, tmA, tmB, tmB3, grid, st);
     g_last_info.launches = 1;
     g_last_info.grid_ctas = grid;
     g_last_info.dispatch_ctas = p.ep_dispatch * ranks;
@@ -585,8 +593,17 @@ extern "C" {
 mk_status_t mk_moe_ep_sim(const void* x, const float* logits, int T, int H, int E, int k, const void* W, int F,
                           int ranks, void* y_tok, int32_t* src_index, int32_t* expert_offsets, float* gate_w,
                           void* out, void* stream, const mk_config_t* cfg, void* workspace, size_t ws_bytes) {
-    return run_ep(x, logits, T, H, E, k, W, F, ranks, y_tok, src_index, expert_offsets, gate_w, out, stream, cfg,
-                  workspace, ws_bytes);
+    return run_ep(x, logits, T, H, E, k, W, nullptr, F, ranks, y_tok, src_index, expert_offsets, gate_w, out, stream,
+                  cfg, workspace, ws_bytes);
+}
+
+mk_status_t mk_moe_ep_sim_gated(const void* x, const float* logits, int T, int H, int E, int k, const void* W1,
+                                const void* W3, int F, int ranks, void* h_tok, int32_t* src_index,
+                                int32_t* expert_offsets, float* gate_w, void* out, void* stream,
+                                const mk_config_t* cfg, void* workspace, size_t ws_bytes) {
+    if (T > 0 && !W3) return MK_ERR_INVALID_ARG;
+    return run_ep(x, logits, T, H, E, k, W1, T > 0 ? W3 : nullptr, F, ranks, h_tok, src_index, expert_offsets,
+                  gate_w, out, stream, cfg, workspace, ws_bytes);
 }
 
 size_t mk_ep_workspace_size(int T, int H, int F, int E, int k, int ranks) {

@@ -1736,7 +1736,8 @@ struct EpMaps {
 };
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-    mk_ep_kernel(const Params p, const __grid_constant__ EpMaps maps, const __grid_constant__ CUtensorMap tmB) {
+    mk_ep_kernel(const Params p, const __grid_constant__ EpMaps maps, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmB3) {
     CtrlSmem* cs = ctrl();
     const uint32_t flag = 1u;
     const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
@@ -1821,7 +1822,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int e0 = rank * epr, e1 = e0 + epr;
             const WorkQueue wq{&me->next_item, cs->item_start[e0], cs->item_start[e1], cs->offs[e0],
                                p.ep_ready[rank], cs->tile_start[e0]};
-            compute_role(p, &maps.a[rank], &tmB, nullptr, cs, wq, false, flag, w);
+            compute_role(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
             stamp(p, 7);
         }
         if (p.combine_out) {
@@ -1952,7 +1953,8 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
     return cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3);
 }
 
-cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& b, int grid, cudaStream_t st) {
+cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& b, const CUtensorMap& b3, int grid,
+                      cudaStream_t st) {
     EpMaps maps{};
     for (int r = 0; r < p.ranks; ++r) maps.a[r] = a[r];
     cudaLaunchConfig_t cfg{};
@@ -1965,7 +1967,7 @@ cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mk_ep_kernel, p, maps, b);
+    return cudaLaunchKernelEx(&cfg, mk_ep_kernel, p, maps, b, b3);
 }
 
 cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,

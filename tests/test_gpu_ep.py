@@ -157,3 +157,44 @@ def test_ep_full_size_equals_single_device(wid, R):
     ref = orc.expert_rows(x, W, w.k, offsets, osrc, rows)
     err = gu.rel_inf(g["y_tok"][osrc[rows]], ref)
     assert err <= gu.Y_TOL[mk.MK_OUT_BF16], f"rel-inf {err:.3e}"
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8])
+def test_ep_gated_equals_single_device_bitwise(R):
+    x, l, W1 = _inputs(1100, 256, 384, 16, 4, seed=61)
+    _, _, W3 = _inputs(1100, 256, 384, 16, 4, seed=62)
+    xd, ld, W1d = gu.to_device(x, l, W1)
+    W3d = gu.to_device(x, l, W3)[2]
+    single = mk.moe_gated(xd, ld, W1d, W3d, 4)
+    g = mk.moe_ep_sim(xd, ld, W1d, 4, R, W3=W3d)
+    torch.cuda.synchronize()
+    order = single["src_index"].long()
+    assert torch.equal(g["src_index"], single["src_index"])
+    assert torch.equal(g["y_tok"][order], single["y_sorted"])
+
+
+def test_ep_gated_combine_against_oracle():
+    T, H, F, E, k = 500, 256, 256, 8, 2
+    x, l, W1 = _inputs(T, H, F, E, k, seed=63)
+    _, _, W3 = _inputs(T, H, F, E, k, seed=64)
+    xd, ld, W1d = gu.to_device(x, l, W1)
+    W3d = gu.to_device(x, l, W3)[2]
+    g = mk.moe_ep_sim(xd, ld, W1d, k, 4, W3=W3d, cfg=mk.make_config(out_dtype=mk.MK_OUT_F32))
+    orc = Oracle()
+    ref = orc.gated_full(x, l, W1, W3, k)
+    ref_out = orc.combine(ref["y"], ref["src_index"], ref["gate_w"], T, k)
+    err = gu.rel_inf(g["out"].cpu().numpy(), ref_out)
+    assert err <= gu.Y_TOL[mk.MK_OUT_F32], f"gated EP combine rel-inf {err:.3e}"
+
+
+def test_ep_gated_full_size_mixtral_like():
+    w = synth.WORKLOADS[2]
+    x, l, W1 = synth.make_inputs(w)
+    W3 = synth.make_w(synth.Workload(w.name, w.T, w.H, w.F, w.E, w.k, w.seed + 7))
+    xd, ld, W1d = gu.to_device(x, l, W1)
+    W3d = gu.to_device(x, l, W3)[2]
+    del W1, W3
+    single = mk.moe_gated(xd, ld, W1d, W3d, w.k)
+    g = mk.moe_ep_sim(xd, ld, W1d, w.k, 8, W3=W3d)
+    torch.cuda.synchronize()
+    assert torch.equal(g["y_tok"][single["src_index"].long()], single["y_sorted"])

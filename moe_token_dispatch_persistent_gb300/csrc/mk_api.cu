@@ -550,8 +550,14 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     p.ep = 1;
     p.ep_cpr = cpr;
     {
-        const int want = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
+        // Every tile waits for the rows of all R sources, so each rank's send
+        // role must be quick: about 64 sending CTAs in all (at most half of a
+        // rank's) measured best or near it on GB300 for R = 2..8; they join
+        // the GEMM once their rows are out.
+        int want = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
+        if (c.dispatch_ctas <= 0 && ranks > 1 && want < 64) want = 64;
         int per = (want + ranks - 1) / ranks;
+        if (c.dispatch_ctas <= 0 && ranks > 1 && per > cpr / 2) per = cpr / 2;
         p.ep_dispatch = per < 1 ? 1 : (per > cpr ? cpr : per);
     }
     p.ep_tile_cap = L.tile_cap;

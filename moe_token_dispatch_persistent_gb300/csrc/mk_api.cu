@@ -183,10 +183,14 @@ int resolve_pair(const mk_config_t& c, int T, int E, int k) {
 // Work order within an expert: whole expert weight reused through L2 when it
 // is small (N-group = all N-blocks, tiles outer); otherwise groups of
 // N-blocks whose weight slice is ~16 MB.
-int n_group_for(int H, int F, int nb) {
+// N-blocks per group of the work order, chosen so the weight slices one
+// group streams stay in L2 while all its tiles use them.  `sharers` groups
+// stream at the same time (the ranks of the expert-parallel simulation, each
+// on its own experts), so they share the budget.
+int n_group_for(int H, int F, int nb, int sharers = 1) {
     const double w_bytes = double(H) * F * 2.0;
-    if (w_bytes <= 32.0 * 1024 * 1024) return nb;
-    int g = int((16.0 * 1024 * 1024) / (double(H) * BN * 2.0));
+    if (w_bytes <= 32.0 * 1024 * 1024 / sharers) return nb;
+    int g = int((16.0 * 1024 * 1024 / sharers) / (double(H) * BN * 2.0));
     if (g < 1) g = 1;
     if (g > nb) g = nb;
     return g;
@@ -523,7 +527,8 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     p.nch = L.nch;
     p.nb = nb;
     p.kblocks = H / BK;
-    p.n_group = c.n_group > 0 ? (c.n_group < nb ? c.n_group : nb) : n_group_for(H, F, nb);
+    // ranks stream their own experts' weights at once, so they share L2
+    p.n_group = c.n_group > 0 ? (c.n_group < nb ? c.n_group : nb) : n_group_for(H, F, nb, ranks);
     p.mode = MK_MODE_FUSED;
     p.compute = 1;
     p.tile_rows = BM;

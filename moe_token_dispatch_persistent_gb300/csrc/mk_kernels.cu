@@ -141,6 +141,18 @@ __device__ __forceinline__ bool wait_eq(const uint32_t* p, uint32_t v, const Wai
     return true;
 }
 
+// The same waits taken by every lane of a warp; the result is the same on
+// every lane (a lane that timed out makes the whole warp give up).
+__device__ __forceinline__ bool warp_wait_mbar(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
+    return __all_sync(0xffffffffu, wait_mbar(bar, parity, w, site));
+}
+__device__ __forceinline__ bool warp_wait_geq(const uint32_t* p, uint32_t target, const WaitCtx& w, int site) {
+    return __all_sync(0xffffffffu, wait_geq(p, target, w, site));
+}
+__device__ __forceinline__ bool warp_wait_eq(const uint32_t* p, uint32_t v, const WaitCtx& w, int site) {
+    return __all_sync(0xffffffffu, wait_eq(p, v, w, site));
+}
+
 __device__ __forceinline__ void stamp(const Params& p, int slot) {
     if (p.trace && threadIdx.x == 0) p.trace_buf[blockIdx.x * TRACE_SLOTS + slot] = globaltimer();
 }
@@ -807,8 +819,10 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
             ok = go == 0;
             break;
         }
+        inf.e = __shfl_sync(0xffffffffu, inf.e, 0);
         inf.row0 = __shfl_sync(0xffffffffu, inf.row0, 0);
         inf.nrows = __shfl_sync(0xffffffffu, inf.nrows, 0);
+        inf.nbk = __shfl_sync(0xffffffffu, inf.nbk, 0);
         // byte offset in x of the tile rows this lane copies (rows past the
         // tile repeat its first row; their products are never stored)
         uint32_t rowoff[COPY_ROWS / 4];
@@ -819,16 +833,12 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
             rowoff[i] = uint32_t(min(max(q / p.k, 0), p.T - 1)) * uint32_t(p.H) * 2u;
         }
         for (int kb = 0; kb < p.kblocks; ++kb) {
-            int okk = 1;
-            if (lane == 0) {
-                if (!wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) okk = 0;
-                else if (leader) mbar_arrive_expect_tx(&cs->full[stage], B_STAGE_BYTES);
-            }
-            okk = __shfl_sync(0xffffffffu, okk, 0);  // also orders lane 0's expect-tx first
-            if (!okk) {
+            if (!warp_wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
                 ok = false;
                 break;
             }
+            if (leader) mbar_arrive_expect_tx_elect(&cs->full[stage], B_STAGE_BYTES);
+            __syncwarp();  // the expect-tx before this warp's copies arrive
             uint64_t* fb = &cs->full[stage];
             uint8_t* a = s + SM_A + stage * A_STAGE_BYTES + cw * COPY_ROWS * 128;
             {
@@ -841,7 +851,7 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
                     cp_async_16_u32(((i & 1) ? d1 - 512 : d0) + 512 * i, src + rowoff[i]);
                 cp_async_mbar_arrive_noinc(fb);
             }
-            if (leader && lane == 0) {
+            if (leader) {
                 uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
                 const int ncol = p.F;
                 if (p.gated) {
@@ -849,14 +859,16 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
                     for (int q = 0; q < GATED_BN / 64; ++q) {
                         const int col = inf.nbk * GATED_BN + q * 64;
                         const int cc = col < ncol ? col : ncol;
-                        tma_load_2d(b + q * B_CHUNK_BYTES, tmB, cc, inf.e * p.H + kb * BK, fb);
-                        tma_load_2d(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, cc, inf.e * p.H + kb * BK, fb);
+                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, cc, inf.e * p.H + kb * BK, fb);
+                        tma_load_2d_elect(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, cc, inf.e * p.H + kb * BK,
+                                          fb);
                     }
                 } else {
 #pragma unroll
                     for (int q = 0; q < BN / 64; ++q) {
                         const int col = inf.nbk * BN + q * 64;
-                        tma_load_2d(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK, fb);
+                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK,
+                                          fb);
                     }
                 }
                 issued_any |= 1u << stage;
@@ -917,168 +929,174 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     if (p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
         producer_direct(p, tmB, tmB3, cs, warp == 0 ? 0 : warp - EPI_WARP_END + 1, wp);
     } else if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer ----------------
-            uint32_t stage = 0, phase = 0;
-            uint32_t issued_par = 0, issued_any = 0;  // per-stage bit: parity of the last issue
-            bool ok = true;
-            uint32_t next = atom_add_relaxed_u32(wq.next, 1u);
-            const int ntiles = cs->tile_start[p.E];
-            for (uint32_t it = 0; ok; ++it) {
-                const int item = wq.lo + int(next);
-                const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
-                if (!wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+        // ---------------- TMA producer: the whole warp runs the loop, one elected lane issues ----------------
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued_par = 0, issued_any = 0;  // per-stage bit: parity of the last issue
+        bool ok = true;
+        uint32_t next = 0;
+        if (lane == 0) next = atom_add_relaxed_u32(wq.next, 1u);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        const int ntiles = cs->tile_start[p.E];
+        for (uint32_t it = 0; ok; ++it) {
+            const int item = wq.lo + int(next);
+            const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+            if (!warp_wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+                ok = false;
+                break;
+            }
+            if (item >= wq.hi) {
+                if (lane == 0) {
+                    cs->info[slot].e = -1;
+                    mbar_arrive(&cs->info_full[slot]);
+                }
+                break;
+            }
+            uint32_t ahead = 0;
+            if (lane == 0) ahead = atom_add_relaxed_u32(wq.next, 1u);  // the next item, claimed one ahead
+            Info inf;
+            int gtile;
+            decode_item(p, cs, item, inf, gtile);
+            const int pf = p.l2_prefetch;
+            if (pf > 0) {
+                // the first k-blocks of this item's weight slice head for L2 now
+                const int n0 = min(pf, p.kblocks);
+                for (int kb = 0; kb < n0; ++kb)
+#pragma unroll
+                    for (int q = 0; q < BN / 64; ++q) {
+                        const int col = inf.nbk * BN + q * 64;
+                        if (col < p.F) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + kb * BK);
+                    }
+            }
+            if (lane == 0) {
+                cs->info[slot] = inf;
+                mbar_arrive(&cs->info_full[slot]);
+            }
+            if (wq.arrived) {
+                // every source's rows of this tile have landed
+                if (!warp_wait_geq(wq.arrived + (gtile - wq.tile_lo), uint32_t(inf.nrows), w, SITE_TILE_READY)) {
                     ok = false;
                     break;
                 }
-                if (item >= wq.hi) {
-                    cs->info[slot].e = -1;
-                    mbar_arrive(&cs->info_full[slot]);
+                fence_proxy_async();
+            } else if (wait_ready) {
+                // one acquire per item until every tile is known to be in
+                if (__all_sync(0xffffffffu, ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles))) {
+                    wait_ready = false;
+                } else if (!warp_wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
+                    ok = false;
                     break;
                 }
-                next = atom_add_relaxed_u32(wq.next, 1u);  // prefetch the next item
-                Info inf;
-                int gtile;
-                decode_item(p, cs, item, inf, gtile);
-                const int pf = p.l2_prefetch;
-                if (pf > 0) {
-                    // the first k-blocks of this item's weight slice head for L2 now
-                    const int n0 = min(pf, p.kblocks);
-                    for (int kb = 0; kb < n0; ++kb)
-#pragma unroll
-                        for (int q = 0; q < BN / 64; ++q) {
-                            const int col = inf.nbk * BN + q * 64;
-                            if (col < p.F) tma_prefetch_l2_2d(tmB, col, inf.e * p.H + kb * BK);
-                        }
+                fence_proxy_async();
+            }
+            const int ncol = p.F;
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (!warp_wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
+                    ok = false;
+                    break;
                 }
-                cs->info[slot] = inf;
-                mbar_arrive(&cs->info_full[slot]);
-                if (wq.arrived) {
-                    // every source's rows of this tile have landed
-                    if (!wait_geq(wq.arrived + (gtile - wq.tile_lo), uint32_t(inf.nrows), w, SITE_TILE_READY)) {
-                        ok = false;
-                        break;
+                if (pf > 0 && kb + pf < p.kblocks) {
+#pragma unroll
+                    for (int q = 0; q < BN / 64; ++q) {
+                        const int col = inf.nbk * BN + q * 64;
+                        if (col < ncol) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + (kb + pf) * BK);
                     }
-                    fence_proxy_async();
-                } else if (wait_ready) {
-                    // one acquire per item until every tile is known to be in
-                    if (ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles)) {
-                        wait_ready = false;
-                    } else if (!wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async();
                 }
-                const int ncol = p.F;
-                for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    if (pf > 0 && kb + pf < p.kblocks) {
+                uint64_t* fb = &cs->full[stage];
+                mbar_arrive_expect_tx_elect(fb, STAGE_BYTES);
+                uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
+                uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
+                tma_load_2d_elect(a, tmA, kb * BK, inf.row0 - wq.a_row0, fb);
+                if (p.gated) {
+                    // 128 columns of W1 into the first half of the B stage, of W3 into the second
 #pragma unroll
-                        for (int q = 0; q < BN / 64; ++q) {
-                            const int col = inf.nbk * BN + q * 64;
-                            if (col < ncol) tma_prefetch_l2_2d(tmB, col, inf.e * p.H + (kb + pf) * BK);
-                        }
+                    for (int q = 0; q < GATED_BN / 64; ++q) {
+                        const int col = inf.nbk * GATED_BN + q * 64;
+                        const int c = col < ncol ? col : ncol;
+                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, c, inf.e * p.H + kb * BK, fb);
+                        tma_load_2d_elect(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, c, inf.e * p.H + kb * BK,
+                                          fb);
                     }
-                    uint64_t* fb = &cs->full[stage];
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
-                    uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
-                    tma_load_2d(a, tmA, kb * BK, inf.row0 - wq.a_row0, fb);
-                    if (p.gated) {
-                        // 128 columns of W1 into the first half of the B stage, of W3 into the second
+                } else {
 #pragma unroll
-                        for (int q = 0; q < GATED_BN / 64; ++q) {
-                            const int col = inf.nbk * GATED_BN + q * 64;
-                            const int c = col < ncol ? col : ncol;
-                            tma_load_2d(b + q * B_CHUNK_BYTES, tmB, c, inf.e * p.H + kb * BK, fb);
-                            tma_load_2d(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, c, inf.e * p.H + kb * BK, fb);
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < BN / 64; ++q) {
-                            const int col = inf.nbk * BN + q * 64;
-                            // chunks past F read as zeros (out of bounds fill)
-                            tma_load_2d(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK,
-                                        fb);
-                        }
+                    for (int q = 0; q < BN / 64; ++q) {
+                        const int col = inf.nbk * BN + q * 64;
+                        // chunks past F read as zeros (out of bounds fill)
+                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol,
+                                          inf.e * p.H + kb * BK, fb);
                     }
-                    issued_any |= 1u << stage;
-                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                }
+                issued_any |= 1u << stage;
+                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            if (!ok) {
-                // let every issued tensor load land before the CTA can exit
-                WaitCtx shortw{nullptr, 0u, 5000000LL};
-                for (int st = 0; st < STAGES; ++st)
-                    if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
-            }
+            next = __shfl_sync(0xffffffffu, ahead, 0);
+        }
+        if (!ok) {
+            // let every issued tensor load land before the CTA can exit
+            WaitCtx shortw{nullptr, 0u, 5000000LL};
+            for (int st = 0; st < STAGES; ++st)
+                if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
-            bool issued = false;
-            for (uint32_t it = 0;; ++it) {
-                const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
-                if (!wait_mbar(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
-                const int e = cs->info[slot].e;
-                mbar_arrive(&cs->info_empty[slot]);
-                if (e < 0) break;
-                if (!wait_mbar(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
-                tc_fence_after();
-                const uint32_t d = cs->tmem_base + acc * BN;
-                bool ok = true;
-                for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!wait_mbar(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    // direct rows were written by cp.async (generic proxy): order
-                    // them before the tensor core reads the stage
-                    if (p.direct) fence_proxy_async_shared();
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(s + SM_A + stage * A_STAGE_BYTES);
-                    const uint32_t b0 = smem_u32(s + SM_B + stage * B_STAGE_BYTES);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // A: K-major, 128B swizzle, 8-row groups 1024 B apart; +32 B per K=16
-                        const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
-                        // B: N-major, 128B swizzle; 64-column chunks 8 KiB apart (LBO),
-                        // 8-row K groups 1024 B apart (SBO); +2 KiB per K=16
-                        // Gated: the stage holds 128 columns of W1 then the same 128
-                        // of W3 as four consecutive 64-column chunks, so one N = 256
-                        // product leaves A.W1 in accumulator columns [0, 128) and
-                        // A.W3 in [128, 256).
-                        const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
-                        tc_mma_f16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    }
-                    issued = true;
-                    tc_commit(&cs->empty[stage]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+        // ---------------- MMA issuer: the whole warp runs the loop, one elected lane issues ----------------
+        uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
+        bool issued = false;
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+            if (!warp_wait_mbar(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
+            const int e = cs->info[slot].e;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cs->info_empty[slot]);
+            if (e < 0) break;
+            if (!warp_wait_mbar(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
+            tc_fence_after();
+            const uint32_t d = cs->tmem_base + acc * BN;
+            bool ok = true;
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (!warp_wait_mbar(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
-                tc_commit(&cs->acc_full[acc]);
-                acc ^= 1u;
-                if (acc == 0) accph ^= 1u;
+                // direct rows were written by cp.async (generic proxy): order
+                // them before the tensor core reads the stage
+                if (p.direct) fence_proxy_async_shared();
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(s + SM_A + stage * A_STAGE_BYTES);
+                const uint32_t b0 = smem_u32(s + SM_B + stage * B_STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    // A: K-major, 128B swizzle, 8-row groups 1024 B apart; +32 B per K=16
+                    const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
+                    // B: N-major, 128B swizzle; 64-column chunks 8 KiB apart (LBO),
+                    // 8-row K groups 1024 B apart (SBO); +2 KiB per K=16
+                    // Gated: the stage holds 128 columns of W1 then the same 128
+                    // of W3 as four consecutive 64-column chunks, so one N = 256
+                    // product leaves A.W1 in accumulator columns [0, 128) and
+                    // A.W3 in [128, 256).
+                    const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
+                    tc_mma_f16_elect(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                }
+                issued = true;
+                tc_commit_elect(&cs->empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            if (issued) {
-                // every MMA this thread issued has completed before TMEM is freed
-                tc_commit(&cs->drain);
-                WaitCtx shortw{nullptr, 0u, 5000000LL};
-                wait_mbar(&cs->drain, 0u, shortw, SITE_DRAIN);
-            }
+            if (!ok) break;
+            tc_commit_elect(&cs->acc_full[acc]);
+            acc ^= 1u;
+            if (acc == 0) accph ^= 1u;
+        }
+        if (issued) {
+            // every MMA this warp issued has completed before TMEM is freed
+            tc_commit_elect(&cs->drain);
+            WaitCtx shortw{nullptr, 0u, 5000000LL};
+            warp_wait_mbar(&cs->drain, 0u, shortw, SITE_DRAIN);
         }
         __syncwarp();
     } else if (warp < EPI_WARP_END) {
@@ -1306,6 +1324,10 @@ __device__ __forceinline__ bool wait_mbar_cl(uint64_t* bar, uint32_t parity, con
     return true;
 }
 
+__device__ __forceinline__ bool warp_wait_mbar_cl(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
+    return __all_sync(0xffffffffu, wait_mbar_cl(bar, parity, w, site));
+}
+
 constexpr uint32_t IDESC_PAIR = umma_idesc_bf16(PAIR_TILE_M, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
 
 // CTA-pair compute role (cluster of two CTAs, cta_group::2): one 256 x 256
@@ -1337,107 +1359,114 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
     }
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- producer (both CTAs) ----------------
-            uint32_t stage = 0, phase = 0;
-            uint32_t issued_par = 0, issued_any = 0;
-            bool ok = true;
-            uint32_t next = leader ? atom_add_relaxed_u32(&p.ctl->next_item, 1u) : 0u;
-            const int ntiles = cs->tile_start[p.E];
-            const uint32_t full_leader = mapa_shared(smem_u32(&cs->full[0]), 0);
-            for (uint32_t it = 0; ok; ++it) {
-                const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
-                Info inf{-1, 0, 0, 0};
-                int gtile = 0;
-                if (leader) {
-                    const int item = int(next);
-                    if (!wait_mbar_cl(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    if (item < total_items) {
-                        next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
-                        decode_item(p, cs, item, inf, gtile);
-                    }
-                    cs->info[slot] = inf;
-                    const uint32_t peer_info = mapa_shared(smem_u32(&cs->info[slot]), 1);
-                    if (peer_info & 15u) {  // self-check: a 16-byte store needs a 16-byte slot
+        // ---------------- producer (both CTAs): the whole warp runs the loop, one elected lane issues ----------------
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued_par = 0, issued_any = 0;
+        bool ok = true;
+        uint32_t next = 0;
+        if (leader && lane == 0) next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        const int ntiles = cs->tile_start[p.E];
+        const uint32_t full_leader = mapa_shared(smem_u32(&cs->full[0]), 0);
+        for (uint32_t it = 0; ok; ++it) {
+            const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+            Info inf{-1, 0, 0, 0};
+            int gtile = 0;
+            uint32_t ahead = 0;
+            if (leader) {
+                const int item = int(next);
+                if (!warp_wait_mbar_cl(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                if (item < total_items) {
+                    if (lane == 0) ahead = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+                    decode_item(p, cs, item, inf, gtile);
+                }
+                const uint32_t peer_info = mapa_shared(smem_u32(&cs->info[slot]), 1);
+                if (peer_info & 15u) {  // self-check: a 16-byte store needs a 16-byte slot
+                    if (lane == 0) {
                         record_error(ERR_FAULT, SITE_PAIR_ALIGN, peer_info);
                         raise_abort(w);
-                        ok = false;
-                        break;
                     }
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    cs->info[slot] = inf;
                     st_cluster_v4(peer_info, inf.e, inf.row0, inf.nrows, inf.nbk);
                     mbar_arrive(&cs->info_full[slot]);
                     mbar_arrive_cluster(mapa_shared(smem_u32(&cs->info_full[slot]), 1));
-                } else {
-                    if (!wait_mbar_cl(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    inf = cs->info[slot];
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&cs->info_empty[slot]), 0));
-                    if (inf.e >= 0) gtile = cs->tile_start[inf.e] + (inf.row0 - cs->offs[inf.e]) / p.tile_rows;
                 }
-                if (inf.e < 0) break;
-                if (wait_ready) {
-                    if (ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles)) {
-                        wait_ready = false;
-                    } else if (!wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async();
+            } else {
+                if (!warp_wait_mbar_cl(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) {
+                    ok = false;
+                    break;
                 }
-                const int arow = inf.row0 + int(rank) * BM;
-                for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!wait_mbar_cl(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    if (leader) mbar_arrive_expect_tx(&cs->full[stage], 2 * (PA_STAGE_BYTES + PB_STAGE_BYTES));
-                    const uint32_t fb = full_leader + stage * uint32_t(sizeof(uint64_t));
-                    tma_load_2d_pair(s + SM_PA + stage * PA_STAGE_BYTES, tmA, kb * BK, arow, fb);
-                    uint8_t* b = s + SM_PB + stage * PB_STAGE_BYTES;
+                inf = cs->info[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&cs->info_empty[slot]), 0));
+                if (inf.e >= 0) gtile = cs->tile_start[inf.e] + (inf.row0 - cs->offs[inf.e]) / p.tile_rows;
+            }
+            if (inf.e < 0) break;
+            if (wait_ready) {
+                if (__all_sync(0xffffffffu, ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles))) {
+                    wait_ready = false;
+                } else if (!warp_wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async();
+            }
+            const int arow = inf.row0 + int(rank) * BM;
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (!warp_wait_mbar_cl(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) mbar_arrive_expect_tx_elect(&cs->full[stage], 2 * (PA_STAGE_BYTES + PB_STAGE_BYTES));
+                const uint32_t fb = full_leader + stage * uint32_t(sizeof(uint64_t));
+                tma_load_2d_pair_elect(s + SM_PA + stage * PA_STAGE_BYTES, tmA, kb * BK, arow, fb);
+                uint8_t* b = s + SM_PB + stage * PB_STAGE_BYTES;
 #pragma unroll
-                    for (int q = 0; q < BN / 128; ++q) {
-                        const int col = inf.nbk * BN + int(rank) * (BN / 2) + q * 64;
-                        tma_load_2d_pair(b + q * B_CHUNK_BYTES, tmB, col < p.F ? col : p.F, inf.e * p.H + kb * BK,
-                                         fb);
-                    }
-                    issued_any |= 1u << stage;
-                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == PSTAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                for (int q = 0; q < BN / 128; ++q) {
+                    const int col = inf.nbk * BN + int(rank) * (BN / 2) + q * 64;
+                    tma_load_2d_pair_elect(b + q * B_CHUNK_BYTES, tmB, col < p.F ? col : p.F, inf.e * p.H + kb * BK,
+                                           fb);
+                }
+                issued_any |= 1u << stage;
+                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == PSTAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            if (!ok && leader) {
-                WaitCtx shortw{nullptr, 0u, 5000000LL};
-                for (int st = 0; st < PSTAGES; ++st)
-                    if (issued_any & (1u << st))
-                        wait_mbar_cl(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
-            }
+            if (leader) next = __shfl_sync(0xffffffffu, ahead, 0);
+        }
+        if (!ok && leader && lane == 0) {
+            WaitCtx shortw{nullptr, 0u, 5000000LL};
+            for (int st = 0; st < PSTAGES; ++st)
+                if (issued_any & (1u << st)) wait_mbar_cl(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (leader && lane == 0) {
-            // ---------------- 2-SM MMA issuer (leader only) ----------------
+        if (leader) {
+            // ---------------- 2-SM MMA issuer (leader's warp 1; one elected lane issues) ----------------
             uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
             bool issued = false;
             for (uint32_t it = 0;; ++it) {
                 const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
-                if (!wait_mbar_cl(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
+                if (!warp_wait_mbar_cl(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
                 const int e = cs->info[slot].e;
-                mbar_arrive(&cs->info_empty[slot]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cs->info_empty[slot]);
                 if (e < 0) break;
-                if (!wait_mbar_cl(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
+                if (!warp_wait_mbar_cl(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
                 tc_fence_after();
                 const uint32_t d = cs->tmem_base + acc * BN;
                 bool ok = true;
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!wait_mbar_cl(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
+                    if (!warp_wait_mbar_cl(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
                         ok = false;
                         break;
                     }
@@ -1449,24 +1478,24 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
                         // the peer's rows / columns sit at the same offsets in its shared memory
                         const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
                         const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
-                        tc_mma_f16_pair(d, ad, bd, IDESC_PAIR, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16_pair_elect(d, ad, bd, IDESC_PAIR, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued = true;
-                    tc_commit_pair_multicast(&cs->empty[stage], 0x3);
+                    tc_commit_pair_multicast_elect(&cs->empty[stage], 0x3);
                     if (++stage == PSTAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit_pair_multicast(&cs->acc_full[acc], 0x3);
+                tc_commit_pair_multicast_elect(&cs->acc_full[acc], 0x3);
                 acc ^= 1u;
                 if (acc == 0) accph ^= 1u;
             }
             if (issued) {
-                tc_commit_pair(&cs->drain);
+                tc_commit_pair_elect(&cs->drain);
                 WaitCtx shortw{nullptr, 0u, 5000000LL};
-                wait_mbar_cl(&cs->drain, 0u, shortw, SITE_DRAIN);
+                warp_wait_mbar_cl(&cs->drain, 0u, shortw, SITE_DRAIN);
             }
         }
         __syncwarp();

@@ -89,8 +89,9 @@ typedef struct mk_config {
     int32_t trace;          /* 1 = record per-CTA %globaltimer phase stamps      */
     int32_t l2_prefetch;    /* W K-blocks prefetched into L2 ahead of use;
                                <= 0 = off (the default)                          */
-    int32_t mma_pair;       /* MK_MMA_*: one SM per 128-row tile, or an SM pair
-                               (cta_group::2) per 256-row tile                  */
+    int32_t mma_pair;       /* MK_MMA_*: one SM per 128-row tile, an SM pair
+                               (cta_group::2) per 256-row tile, or one SM per
+                               256-row tile with two accumulators (WIDE)     */
     int32_t gather;         /* MK_GATHER_*: where the GEMM's token rows come from */
     int32_t reserved[4];    /* must be zero                                     */
 } mk_config_t;
@@ -107,8 +108,14 @@ enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
 /* Expert GEMM tile.  SINGLE: each CTA runs a 128 x 256 tile alone.  PAIR: a
  * cluster of two CTAs (two SMs) runs a 256 x 256 tile with the 2-SM tensor
  * core instruction; each SM stages half the operands, so the same shared
- * memory holds six stages instead of four.  AUTO picks per shape. */
-enum { MK_MMA_AUTO = 0, MK_MMA_SINGLE = 1, MK_MMA_PAIR = 2 };
+ * memory holds six stages instead of four.  WIDE: each CTA runs a 256 x 256
+ * tile alone, as two 128-row accumulators that share every staged block of
+ * the weights (three stages of 64 KiB; an expert's last tile of at most 128
+ * rows uses one accumulator); staged rows only (not with
+ * MK_GATHER_DIRECT), single-device calls only.  AUTO: WIDE for the plain
+ * expert FFN with staged rows when T*k >= 256*E (two or more 128-row tiles
+ * per expert on average), SINGLE otherwise. */
+enum { MK_MMA_AUTO = 0, MK_MMA_SINGLE = 1, MK_MMA_PAIR = 2, MK_MMA_WIDE = 3 };
 
 /* Per-launch facts, for tests and the benchmark. */
 typedef struct mk_launch_info {
@@ -117,7 +124,7 @@ typedef struct mk_launch_info {
     int32_t launches;       /* kernels launched by the last call      */
     int32_t n_group;
     int64_t workspace_bytes;
-    int32_t mma_pair;       /* MK_MMA_SINGLE or MK_MMA_PAIR as resolved */
+    int32_t mma_pair;       /* MK_MMA_SINGLE, MK_MMA_PAIR or MK_MMA_WIDE as resolved */
     int32_t gather;         /* MK_GATHER_STAGED or MK_GATHER_DIRECT as resolved */
 } mk_launch_info_t;
 

@@ -34,6 +34,7 @@ MK_FAULT_DROP_TILE_FLAG = 1
 MK_MMA_AUTO = 0
 MK_MMA_SINGLE = 1
 MK_MMA_PAIR = 2
+MK_MMA_WIDE = 3
 MK_GATHER_AUTO = 0
 MK_GATHER_STAGED = 1
 MK_GATHER_DIRECT = 2

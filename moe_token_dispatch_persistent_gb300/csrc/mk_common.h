@@ -45,6 +45,11 @@ constexpr int SM_PA = 0;
 constexpr int SM_PB = SM_PA + PSTAGES * PA_STAGE_BYTES;    // 96 KiB
 constexpr int MAX_STAGES = PSTAGES > STAGES ? PSTAGES : STAGES;
 
+// Wide variant (one SM, 256-row tiles, two accumulators sharing each B
+// stage): a stage holds 2 x 16 KiB of A and 32 KiB of B, so three fit.
+constexpr int WIDE_TILE_M = 2 * BM;
+constexpr int WSTAGES = 3;
+
 // Dynamic shared memory map (offsets from a 1024-byte aligned base).
 constexpr int SM_A = 0;
 constexpr int SM_B = SM_A + STAGES * A_STAGE_BYTES;           // 64 KiB
@@ -152,9 +157,10 @@ struct Params {
     int debug_drop_tile;     // tile whose flag is withheld (-1: none)
     int l2_prefetch;         // W k-blocks prefetched into L2 ahead of the TMA loads (0: off)
     int pair;                // 1: 2-SM MMA (cluster of 2 CTAs per 256-row tile)
+    int wide;                // 1: 256-row tiles on one SM, two accumulators sharing each B stage
     int gated;               // 1: y = silu(x.W1) * (x.W3), 128-column N-blocks
     int direct;              // 1: the GEMM's producer copies token rows from x (no staging rows)
-    int tile_rows;           // rows per tile: 128, or 256 with pair
+    int tile_rows;           // rows per tile: 128, or 256 with pair or wide
     int trace;
     long long spin_limit_ns;
     // workspace

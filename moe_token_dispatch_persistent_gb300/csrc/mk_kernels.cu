@@ -916,9 +916,24 @@ __device__ __forceinline__ int rank_of_token(const Params& p, int t) {
 
 // Warp-specialised expert GEMM over work items (tile, N-block) taken from the
 // queue until it is empty.  wait_ready: spin on the tile's flag first.
+//
+// WIDE: 256-row tiles on one SM.  Each stage holds the tile's two 128-row A
+// blocks and one B block; two 128 x 256 accumulators (all 512 TMEM columns)
+// share that B block, so a stage carries 64 KiB for 1024 cycles of MMA
+// instead of 48 KiB for 512.  With TMEM full, the accumulators are
+// single-buffered: the next item's MMAs wait until the epilogue has read
+// both.  A tile of at most 128 rows (an expert's last) uses one accumulator
+// and loads one A block.
+template <bool WIDE>
 __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmB3,
                              CtrlSmem* cs, const WorkQueue& wq,
                              bool wait_ready, uint32_t flag, const WaitCtx& w) {
+    constexpr int NST = WIDE ? WSTAGES : STAGES;
+    constexpr int ASB = WIDE ? 2 * A_STAGE_BYTES : A_STAGE_BYTES;  // A bytes of a stage
+    constexpr int SMA = 0, SMB = NST * ASB;
+    constexpr uint32_t NACC = WIDE ? 1u : 2u;  // accumulator buffers
+    static_assert(SMB + NST * B_STAGE_BYTES <= SM_STAGE_END, "stages must fit in the stage area");
+    static_assert(NST <= MAX_STAGES, "one full/empty barrier pair per stage");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* s = smem_base();
     // Waits inside the pipeline only stall because something upstream (a
@@ -926,7 +941,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     // that times out and is recorded is the one at the root.
     const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
 
-    if (p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
+    if (!WIDE && p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
         producer_direct(p, tmB, tmB3, cs, warp == 0 ? 0 : warp - EPI_WARP_END + 1, wp);
     } else if (warp == 0) {
         // ---------------- TMA producer: the whole warp runs the loop, one elected lane issues ----------------
@@ -1002,10 +1017,12 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     }
                 }
                 uint64_t* fb = &cs->full[stage];
-                mbar_arrive_expect_tx_elect(fb, STAGE_BYTES);
-                uint8_t* a = s + SM_A + stage * A_STAGE_BYTES;
-                uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
+                const bool two = WIDE && inf.nrows > BM;  // second 128-row A block
+                mbar_arrive_expect_tx_elect(fb, two ? STAGE_BYTES + A_STAGE_BYTES : STAGE_BYTES);
+                uint8_t* a = s + SMA + stage * ASB;
+                uint8_t* b = s + SMB + stage * B_STAGE_BYTES;
                 tma_load_2d_elect(a, tmA, kb * BK, inf.row0 - wq.a_row0, fb);
+                if (two) tma_load_2d_elect(a + A_STAGE_BYTES, tmA, kb * BK, inf.row0 - wq.a_row0 + BM, fb);
                 if (p.gated) {
                     // 128 columns of W1 into the first half of the B stage, of W3 into the second
 #pragma unroll
@@ -1027,7 +1044,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 }
                 issued_any |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) {
+                if (++stage == NST) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -1037,7 +1054,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
         if (!ok) {
             // let every issued tensor load land before the CTA can exit
             WaitCtx shortw{nullptr, 0u, 5000000LL};
-            for (int st = 0; st < STAGES; ++st)
+            for (int st = 0; st < NST; ++st)
                 if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
         }
         __syncwarp();
@@ -1049,11 +1066,13 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
             if (!warp_wait_mbar(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
             const int e = cs->info[slot].e;
+            const bool two = WIDE && cs->info[slot].nrows > BM;
             __syncwarp();
             if (lane == 0) mbar_arrive(&cs->info_empty[slot]);
             if (e < 0) break;
             if (!warp_wait_mbar(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
             tc_fence_after();
+            // WIDE: rows 0-127 in TMEM columns [0, 256), rows 128-255 in [256, 512)
             const uint32_t d = cs->tmem_base + acc * BN;
             bool ok = true;
             for (int kb = 0; kb < p.kblocks; ++kb) {
@@ -1065,8 +1084,8 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 // them before the tensor core reads the stage
                 if (p.direct) fence_proxy_async_shared();
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(s + SM_A + stage * A_STAGE_BYTES);
-                const uint32_t b0 = smem_u32(s + SM_B + stage * B_STAGE_BYTES);
+                const uint32_t a0 = smem_u32(s + SMA + stage * ASB);
+                const uint32_t b0 = smem_u32(s + SMB + stage * B_STAGE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // A: K-major, 128B swizzle, 8-row groups 1024 B apart; +32 B per K=16
@@ -1079,18 +1098,23 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     // A.W3 in [128, 256).
                     const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
                     tc_mma_f16_elect(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    if (two)  // the second A block against the same B chunk
+                        tc_mma_f16_elect(d + BN, umma_desc_sw128(a0 + A_STAGE_BYTES + kk * 32, 16, 1024), bd, IDESC,
+                                         (kb | kk) != 0 ? 1u : 0u);
                 }
                 issued = true;
                 tc_commit_elect(&cs->empty[stage]);
-                if (++stage == STAGES) {
+                if (++stage == NST) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
             tc_commit_elect(&cs->acc_full[acc]);
-            acc ^= 1u;
-            if (acc == 0) accph ^= 1u;
+            if (++acc == NACC) {
+                acc = 0;
+                accph ^= 1u;
+            }
         }
         if (issued) {
             // every MMA this warp issued has completed before TMEM is freed
@@ -1112,73 +1136,79 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             if (inf.e < 0) break;
             if (!wait_mbar(&cs->acc_full[acc], accph, wp, SITE_ACC_FULL)) break;
             tc_fence_after();
-            const int rloc = quad * 32 + lane;
-            const bool rowok = rloc < inf.nrows;
-            // expert parallel: the result goes back to the sending rank, into
-            // its return rows in (t, j) order
-            const int ep_q = (p.ep && rowok) ? __ldcg(p.src_index + inf.row0 + rloc) : -1;
-            const size_t row = p.ep ? size_t(ep_q < 0 ? 0 : ep_q) : size_t(inf.row0) + rloc;
-            const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + acc * BN;
-            if (p.gated) {
-                const int n0 = inf.nbk * GATED_BN;
+            // WIDE: the tile's second 128 rows come from the second accumulator
+            const int halves = (WIDE && inf.nrows > BM) ? 2 : 1;
+            for (int half = 0; half < halves; ++half) {
+                const int rloc = half * BM + quad * 32 + lane;
+                const bool rowok = rloc < inf.nrows;
+                // expert parallel: the result goes back to the sending rank, into
+                // its return rows in (t, j) order
+                const int ep_q = (p.ep && rowok) ? __ldcg(p.src_index + inf.row0 + rloc) : -1;
+                const size_t row = p.ep ? size_t(ep_q < 0 ? 0 : ep_q) : size_t(inf.row0) + rloc;
+                const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + (acc + half) * BN;
+                if (p.gated) {
+                    const int n0 = inf.nbk * GATED_BN;
 #pragma unroll 1
-                for (int cc = 0; cc < GATED_BN / 32; ++cc) {
-                    const int col = n0 + cc * 32;
-                    if (col >= p.F) break;
-                    uint32_t r[32], r3[32];
-                    tmem_ld_32x32b_x32(tbase + cc * 32, r);
-                    tmem_ld_32x32b_x32(tbase + GATED_BN + cc * 32, r3);
-                    tmem_ld_wait();
+                    for (int cc = 0; cc < GATED_BN / 32; ++cc) {
+                        const int col = n0 + cc * 32;
+                        if (col >= p.F) break;
+                        uint32_t r[32], r3[32];
+                        tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                        tmem_ld_32x32b_x32(tbase + GATED_BN + cc * 32, r3);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        // SwiGLU: silu(a) * b, silu(a) = a / (1 + e^-a)
-                        const float a = __uint_as_float(r[i]);
-                        r[i] = __float_as_uint(a / (1.f + expf(-a)) * __uint_as_float(r3[i]));
+                        for (int i = 0; i < 32; ++i) {
+                            // SwiGLU: silu(a) * b, silu(a) = a / (1 + e^-a)
+                            const float a = __uint_as_float(r[i]);
+                            r[i] = __float_as_uint(a / (1.f + expf(-a)) * __uint_as_float(r3[i]));
+                        }
+                        if (rowok) store_row32(p, row, col, r);
                     }
-                    if (rowok) store_row32(p, row, col, r);
-                }
-            } else {
-                const int n0 = inf.nbk * BN;
+                } else {
+                    const int n0 = inf.nbk * BN;
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    const int col = n0 + cc * 32;
-                    if (col >= p.F) break;
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + cc * 32, r);
-                    tmem_ld_wait();
-                    if (rowok) store_row32(p, row, col, r);
+                    for (int cc = 0; cc < BN / 32; ++cc) {
+                        const int col = n0 + cc * 32;
+                        if (col >= p.F) break;
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                        tmem_ld_wait();
+                        if (rowok) store_row32(p, row, col, r);
+                    }
                 }
-            }
-            if (p.ep) {
-                // one count per (warp, sending rank): this item's rows are stored
-                const int src = ep_q >= 0 ? rank_of_token(p, ep_q / p.k) : -1;
-                __threadfence();  // this lane's stores before the count that publishes them
-                __syncwarp();
-                const uint32_t peers = __match_any_sync(0xffffffffu, src);
-                if (src >= 0 && lane == __ffs(peers) - 1)
-                    atom_add_acq_rel_u32(&p.ep_ctl[src]->ret_done, uint32_t(__popc(peers)));
-            }
-            if (p.stream_done) {
-                // streamed results: count this item's stored rows per chunk; the
-                // warp that completes a chunk raises its flag for the copy stream
-                const int c = rowok ? int(row / uint32_t(p.stream_rows)) : -1;
-                __threadfence();  // this lane's stores before the count that publishes them
-                __syncwarp();
-                const uint32_t peers = __match_any_sync(0xffffffffu, c);
-                if (c >= 0 && lane == __ffs(peers) - 1) {
-                    const uint32_t n = uint32_t(__popc(peers));
-                    const uint32_t target =
-                        uint32_t(min(p.rows - c * p.stream_rows, p.stream_rows)) * uint32_t(p.nb);
-                    if (atom_add_acq_rel_u32(&p.stream_done[c], n) + n == target) {
-                        __threadfence_system();
-                        st_release_sys_u32(&p.stream_flag[c], p.stream_seq);
+                if (p.ep) {
+                    // one count per (warp, sending rank): this item's rows are stored
+                    const int src = ep_q >= 0 ? rank_of_token(p, ep_q / p.k) : -1;
+                    __threadfence();  // this lane's stores before the count that publishes them
+                    __syncwarp();
+                    const uint32_t peers = __match_any_sync(0xffffffffu, src);
+                    if (src >= 0 && lane == __ffs(peers) - 1)
+                        atom_add_acq_rel_u32(&p.ep_ctl[src]->ret_done, uint32_t(__popc(peers)));
+                }
+                if (p.stream_done) {
+                    // streamed results: count this item's stored rows per chunk; the
+                    // warp that completes a chunk raises its flag for the copy stream
+                    const int c = rowok ? int(row / uint32_t(p.stream_rows)) : -1;
+                    __threadfence();  // this lane's stores before the count that publishes them
+                    __syncwarp();
+                    const uint32_t peers = __match_any_sync(0xffffffffu, c);
+                    if (c >= 0 && lane == __ffs(peers) - 1) {
+                        const uint32_t n = uint32_t(__popc(peers));
+                        const uint32_t target =
+                            uint32_t(min(p.rows - c * p.stream_rows, p.stream_rows)) * uint32_t(p.nb);
+                        if (atom_add_acq_rel_u32(&p.stream_done[c], n) + n == target) {
+                            __threadfence_system();
+                            st_release_sys_u32(&p.stream_flag[c], p.stream_seq);
+                        }
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&cs->acc_empty[acc]);
-            acc ^= 1u;
-            if (acc == 0) accph ^= 1u;
+            if (++acc == NACC) {
+                acc = 0;
+                accph ^= 1u;
+            }
         }
     }
 }
@@ -1730,7 +1760,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (cs->bcast[2]) {
             stamp(p, 6);
             if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, true, flag, w);
-            else compute_role(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), !p.direct, flag, w);
+            else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), true, flag, w);
+            else compute_role<false>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), !p.direct, flag, w);
             stamp(p, 7);
         }
     }
@@ -1851,7 +1882,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int e0 = rank * epr, e1 = e0 + epr;
             const WorkQueue wq{&me->next_item, cs->item_start[e0], cs->item_start[e1], cs->offs[e0],
                                p.ep_ready[rank], cs->tile_start[e0]};
-            compute_role(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
+            compute_role<false>(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
             stamp(p, 7);
         }
         if (p.combine_out) {
@@ -1940,7 +1971,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     build_tables(p, cs);
     __syncthreads();
     if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, false, flag, w);
-    else compute_role(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), false, flag, w);
+    else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), false, flag, w);
+    else compute_role<false>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), false, flag, w);
     cta_teardown<PAIR>(p, cs, true);
 }
 

@@ -295,6 +295,9 @@ def dispatch_bytes(w: synth.Workload) -> int:
     return w.T * w.E * 4 + 2 * w.rows * w.H * 2 + w.rows * 8 + (w.E + 1) * 4
 
 
+TILE_NAMES = {1: "128-row", 2: "256-row on SM pairs", 3: "256-row (two accumulators per SM)"}
+
+
 def compulsory_bytes(w: synth.Workload, active_experts: int) -> int:
     """x + logits + active experts' W + y_sorted (bf16) + src_index + gate_w + offsets."""
     return (w.T * w.H * 2 + w.T * w.E * 4 + active_experts * w.H * w.F * 2 + w.rows * w.F * 2 + w.rows * 8
@@ -397,6 +400,7 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(w, {"mode": "fused persistent", "grid_ctas": info["grid_ctas"],
                                       "dispatch_ctas": info["dispatch_ctas"], "n_group": info["n_group"],
+                                      "tiles": TILE_NAMES.get(info["mma_pair"], str(info["mma_pair"])),
                                       "active_experts": active}),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"bf16_tflops (burst), {peaks_src}",

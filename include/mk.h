@@ -112,9 +112,9 @@ enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
  * tile alone, as two 128-row accumulators that share every staged block of
  * the weights (three stages of 64 KiB; an expert's last tile of at most 128
  * rows uses one accumulator); staged rows only (not with
- * MK_GATHER_DIRECT), single-device calls only.  AUTO: WIDE for the plain
- * expert FFN with staged rows when T*k >= 256*E (two or more 128-row tiles
- * per expert on average), SINGLE otherwise. */
+ * MK_GATHER_DIRECT), single-device calls only.  AUTO: WIDE with staged rows
+ * when T*k >= 256*E (two or more 128-row tiles per expert on average),
+ * SINGLE otherwise. */
 enum { MK_MMA_AUTO = 0, MK_MMA_SINGLE = 1, MK_MMA_PAIR = 2, MK_MMA_WIDE = 3 };
 
 /* Per-launch facts, for tests and the benchmark. */

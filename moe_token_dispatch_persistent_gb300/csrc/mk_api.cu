@@ -172,15 +172,13 @@ int resolve_gather(const mk_config_t& c) {
 }
 
 // Tile height.  AUTO: 256-row tiles on one SM (WIDE) when the average expert
-// holds at least two 128-row tiles and the expert FFN is the plain one;
-// 128-row tiles otherwise.  Measured on GB300 with staged rows: WIDE is 5-8%
-// faster on the Mixtral-like, skewed and imbalanced workloads, 2% slower on
-// decode (4 rows per expert), and slower for the gated FFN, whose heavier
-// epilogue is exposed once the accumulators are single-buffered.  SM pairs
-// only when asked.
-int resolve_pair(const mk_config_t& c, int T, int E, int k, bool gated, bool direct) {
+// holds at least two 128-row tiles; 128-row tiles otherwise.  Measured on
+// GB300 with staged rows: WIDE is 5-14% faster on the Mixtral-like, skewed
+// and imbalanced workloads (plain and gated FFN), 2% slower on decode (4
+// rows per expert).  SM pairs only when asked.
+int resolve_pair(const mk_config_t& c, int T, int E, int k, bool direct) {
     if (c.mma_pair != MK_MMA_AUTO) return c.mma_pair;
-    if (gated || direct || c.mode == MK_MODE_DISPATCH_ONLY) return MK_MMA_SINGLE;
+    if (direct || c.mode == MK_MODE_DISPATCH_ONLY) return MK_MMA_SINGLE;
     return int64_t(T) * k >= int64_t(2 * BM) * E ? MK_MMA_WIDE : MK_MMA_SINGLE;
 }
 
@@ -321,7 +319,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     }
 
     const bool direct = resolve_gather(c) == MK_GATHER_DIRECT;
-    const int mma = resolve_pair(c, T, E, k, W3 != nullptr, direct);
+    const int mma = resolve_pair(c, T, E, k, direct);
     const bool pair = mma == MK_MMA_PAIR, wide = mma == MK_MMA_WIDE;
     if (pair && W3) return MK_ERR_UNSUPPORTED;  // the gated FFN runs on single-SM tiles
     if (direct && (pair || wide)) return MK_ERR_UNSUPPORTED;  // 256-row tiles load staged rows only

@@ -467,10 +467,10 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
     if (c.debug_fault != MK_FAULT_NONE && c.debug_fault != MK_FAULT_DROP_TILE_FLAG) return MK_ERR_INVALID_ARG;
     if (c.dispatch_ctas < 0 || c.grid_ctas < 0 || c.n_group < 0 || c.spin_limit_ns < 0) return MK_ERR_INVALID_ARG;
-    // one fused launch, staged rows, single-SM tiles
-    if (c.mode != MK_MODE_FUSED || c.gather == MK_GATHER_DIRECT || c.mma_pair == MK_MMA_PAIR ||
-        c.mma_pair == MK_MMA_WIDE)
+    // one fused launch, staged rows, tiles on one SM (128-row or wide)
+    if (c.mode != MK_MODE_FUSED || c.gather == MK_GATHER_DIRECT || c.mma_pair == MK_MMA_PAIR)
         return MK_ERR_UNSUPPORTED;
+    const bool wide = resolve_pair(c, T, E, k, false) == MK_MMA_WIDE;
     if (!expert_offsets || !aligned(expert_offsets, 4)) return MK_ERR_INVALID_ARG;
     if (T > 0) {
         if (!x || !logits || !W || !y_tok || !src_index || !gate_w) return MK_ERR_INVALID_ARG;
@@ -536,7 +536,8 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     p.n_group = c.n_group > 0 ? (c.n_group < nb ? c.n_group : nb) : n_group_for(H, F, nb, ranks);
     p.mode = MK_MODE_FUSED;
     p.compute = 1;
-    p.tile_rows = BM;
+    p.wide = wide ? 1 : 0;
+    p.tile_rows = wide ? WIDE_TILE_M : BM;
     {
         int slots = int((SM_STAGE_END) / (size_t(H) * 2));
         p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
@@ -596,7 +597,7 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     g_last_info.grid_ctas = grid;
     g_last_info.dispatch_ctas = p.ep_dispatch * ranks;
     g_last_info.n_group = p.n_group;
-    g_last_info.mma_pair = MK_MMA_SINGLE;
+    g_last_info.mma_pair = wide ? MK_MMA_WIDE : MK_MMA_SINGLE;
     g_last_info.gather = MK_GATHER_STAGED;
     g_last_info.workspace_bytes = int64_t(L.total);
     return err == cudaSuccess ? MK_OK : MK_ERR_CUDA;

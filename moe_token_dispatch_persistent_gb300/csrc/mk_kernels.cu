@@ -1885,7 +1885,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int e0 = rank * epr, e1 = e0 + epr;
             const WorkQueue wq{&me->next_item, cs->item_start[e0], cs->item_start[e1], cs->offs[e0],
                                p.ep_ready[rank], cs->tile_start[e0]};
-            compute_role<false>(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
+            if (p.wide) compute_role<true>(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
+            else compute_role<false>(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
             stamp(p, 7);
         }
         if (p.combine_out) {

@@ -187,13 +187,25 @@ def test_wide_full_size_equals_single(wid):
     assert err <= gu.Y_TOL[mk.MK_OUT_BF16], f"rel-inf {err:.3e}"
 
 
-def test_wide_unsupported_with_direct_rows_and_expert_parallel():
+def test_wide_unsupported_with_direct_rows():
     T, H, F, E, k = 64, 64, 64, 4, 2
     xd, ld, Wd = gu.to_device(*_inputs(T, H, F, E, k))
     o = mk.alloc_outputs(T, F, E, k)
     st = mk.mk_moe_dispatch_gemm_ex(xd, ld, T, H, E, k, Wd, F, o["y_sorted"], o["src_index"], o["expert_offsets"],
                                     o["gate_w"], None, mk.make_config(mma_pair=WIDE, gather=mk.MK_GATHER_DIRECT))
     assert st == mk.MK_ERR_UNSUPPORTED
-    st = mk.mk_moe_ep_sim(xd, ld, T, H, E, k, Wd, F, 2, o["y_sorted"], o["src_index"], o["expert_offsets"],
-                          o["gate_w"], None, None, mk.make_config(mma_pair=WIDE))
-    assert st == mk.MK_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8])
+def test_wide_expert_parallel_bitwise(R):
+    """The expert-parallel simulation on wide tiles: the same bits as the
+    single-device path on 128-row tiles, tokens returned to their ranks."""
+    x, l, W = gu.to_device(*_inputs(1500, 256, 512, 16, 4, seed=21))
+    single = mk.moe_layer(x, l, W, 4, cfg=mk.make_config(mma_pair=mk.MK_MMA_SINGLE))
+    g = mk.moe_ep_sim(x, l, W, 4, R, cfg=mk.make_config(mma_pair=WIDE))
+    torch.cuda.synchronize()
+    assert mk.mk_last_launch_info()["mma_pair"] == WIDE
+    order = single["src_index"].long()
+    assert torch.equal(g["src_index"], single["src_index"])
+    assert torch.equal(g["y_tok"][order], single["y_sorted"])
+    assert torch.equal(g["out"], single["out"])

@@ -102,7 +102,7 @@ typedef struct mk_config {
  * producer warp copies each tile's rows straight from x into its
  * shared-memory stages (16-byte cp.async), so there is no staging copy, no
  * gather role, and the workspace holds no staging rows (T*k*H*2 bytes
- * less); single-SM tiles only, and T*H*2 < 4 GiB.  AUTO = STAGED. */
+ * less); 128-row tiles only, and T*H*2 < 4 GiB.  AUTO = STAGED. */
 enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
 
 /* Expert GEMM tile.  SINGLE: each CTA runs a 128 x 256 tile alone.  PAIR: a
@@ -112,7 +112,7 @@ enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
  * tile alone, as two 128-row accumulators that share every staged block of
  * the weights (three stages of 64 KiB; an expert's last tile of at most 128
  * rows uses one accumulator); staged rows only (not with
- * MK_GATHER_DIRECT), single-device calls only.  AUTO: WIDE with staged rows
+ * MK_GATHER_DIRECT).  AUTO: WIDE with staged rows
  * when T*k >= 256*E (two or more 128-row tiles per expert on average),
  * SINGLE otherwise. */
 enum { MK_MMA_AUTO = 0, MK_MMA_SINGLE = 1, MK_MMA_PAIR = 2, MK_MMA_WIDE = 3 };
@@ -171,9 +171,10 @@ mk_status_t mk_moe_dispatch_gemm_combine(const void* x, const float* logits, int
  *   h_sorted[r,:] = silu(x[t,:] . W1[e]) * (x[t,:] . W3[e]),  silu(a) = a / (1 + e^-a),
  * both products accumulated in fp32 in the same tensor-core pass (the A tile
  * is shared; 128 columns of each projection per work item) and the SwiGLU
- * applied in the epilogue (fp32 expf) before rounding to bf16 (or f32 with
- * MK_OUT_F32).  W1, W3: [E,H,F] bf16, device, 16-byte aligned.  Runs on
- * single-SM tiles (MK_MMA_PAIR returns MK_ERR_UNSUPPORTED).  Other
+ * applied in the epilogue (fp32, fast exponential and divide) before
+ * rounding to bf16 (or f32 with MK_OUT_F32).  W1, W3: [E,H,F] bf16, device,
+ * 16-byte aligned.  Runs on tiles of one SM, 128-row or wide (MK_MMA_PAIR
+ * returns MK_ERR_UNSUPPORTED).  Other
  * arguments and outputs as for mk_moe_dispatch_gemm_ex. */
 mk_status_t mk_moe_dispatch_gated(const void* x, const float* logits, int T, int H, int E, int k, const void* W1,
                                   const void* W3, int F, void* h_sorted, int32_t* src_index,
@@ -205,7 +206,8 @@ mk_status_t mk_moe_dispatch_gated(const void* x, const float* logits, int T, int
  *     expert_offsets[(q+1)*E/R])).
  *   out[T,F] (optional, may be NULL): sum_j gate[t,j] * y_tok[t*k+j], fp32
  *     in slot order, in y_tok's dtype.
- * Supported: MK_MODE_FUSED, staged rows, single-SM tiles; other choices
+ * Supported: MK_MODE_FUSED, staged rows, tiles of one SM (128-row or
+ * wide, resolved as for the single-device call); other choices
  * return MK_ERR_UNSUPPORTED.  cfg.trace records nothing here.  workspace:
  * NULL (library cache, zeroed when allocated) or mk_ep_workspace_size()
  * bytes, 256-byte aligned, zero-filled before its first use, and used by

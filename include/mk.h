@@ -102,7 +102,9 @@ typedef struct mk_config {
  * producer warp copies each tile's rows straight from x into its
  * shared-memory stages (16-byte cp.async), so there is no staging copy, no
  * gather role, and the workspace holds no staging rows (T*k*H*2 bytes
- * less); 128-row tiles only, and T*H*2 < 4 GiB.  AUTO = STAGED. */
+ * less); 128-row or wide tiles (not SM pairs), and T*H*2 < 4 GiB.  AUTO:
+ * DIRECT when k >= 4 and T*k >= 256*E (wide tiles), with cfg.mma_pair AUTO
+ * or WIDE and T*H*2 < 4 GiB; STAGED otherwise. */
 enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
 
 /* Expert GEMM tile.  SINGLE: each CTA runs a 128 x 256 tile alone.  PAIR: a

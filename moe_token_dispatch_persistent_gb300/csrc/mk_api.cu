@@ -160,26 +160,34 @@ int dispatch_split(int grid, int T, int H, int F, int k) {
     return d;
 }
 
+// Average expert rows fill at least two 128-row tiles.
+bool wide_shape(int T, int E, int k) { return int64_t(T) * k >= int64_t(2 * BM) * E; }
+
 // Where the GEMM's token rows come from.  STAGED: the dispatch role copies
 // them into expert-contiguous tiles and flags each tile.  DIRECT: the GEMM's
-// producer warp copies them from x itself (no staging rows in the
+// producer warps copy them from x themselves (no staging rows in the
 // workspace, no gather role).  Dispatch-only always stages (it measures the
-// gather); AUTO stages (measured on GB300: direct is at par on the skewed
-// and imbalanced workloads and slower on the Mixtral-like one).
-int resolve_gather(const mk_config_t& c) {
+// gather).  AUTO: DIRECT for fine-grained routing (k >= 4) on wide tiles,
+// where staging would copy T*k rows of x (0.9-1.1 GB on the skewed and
+// imbalanced workloads) and direct rows measured 13-15% faster on GB300;
+// STAGED otherwise (the Mixtral-like layer, k = 2, runs 2% faster staged).
+int resolve_gather(const mk_config_t& c, int T, int H, int E, int k) {
     if (c.mode == MK_MODE_DISPATCH_ONLY) return MK_GATHER_STAGED;
-    return c.gather == MK_GATHER_DIRECT ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
+    if (c.gather != MK_GATHER_AUTO) return c.gather == MK_GATHER_DIRECT ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
+    if (c.mma_pair == MK_MMA_PAIR || c.mma_pair == MK_MMA_SINGLE) return MK_GATHER_STAGED;
+    const bool fits = uint64_t(T) * uint64_t(H) * 2 < (uint64_t(1) << 32);  // 32-bit row offsets into x
+    return (k >= 4 && wide_shape(T, E, k) && fits) ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
 }
 
 // Tile height.  AUTO: 256-row tiles on one SM (WIDE) when the average expert
 // holds at least two 128-row tiles; 128-row tiles otherwise.  Measured on
-// GB300 with staged rows: WIDE is 5-14% faster on the Mixtral-like, skewed
-// and imbalanced workloads (plain and gated FFN), 2% slower on decode (4
-// rows per expert).  SM pairs only when asked.
-int resolve_pair(const mk_config_t& c, int T, int E, int k, bool direct) {
+// GB300: WIDE is 5-14% faster on the Mixtral-like, skewed and imbalanced
+// workloads (plain and gated FFN) with staged rows, 15-23% with direct rows,
+// and 2% slower on decode (4 rows per expert).  SM pairs only when asked.
+int resolve_pair(const mk_config_t& c, int T, int E, int k) {
     if (c.mma_pair != MK_MMA_AUTO) return c.mma_pair;
-    if (direct || c.mode == MK_MODE_DISPATCH_ONLY) return MK_MMA_SINGLE;
-    return int64_t(T) * k >= int64_t(2 * BM) * E ? MK_MMA_WIDE : MK_MMA_SINGLE;
+    if (c.mode == MK_MODE_DISPATCH_ONLY) return MK_MMA_SINGLE;
+    return wide_shape(T, E, k) ? MK_MMA_WIDE : MK_MMA_SINGLE;
 }
 
 // Work order within an expert: whole expert weight reused through L2 when it
@@ -261,7 +269,7 @@ size_t mk_workspace_size(int T, int H, int F, int E, int k, const mk_config_t* c
     (void)cfg;
     if (validate_sizes(T, H, E, k, F) != MK_OK) return 0;
     const mk_config_t c = config_or_default(cfg);
-    return ws_layout(T, H, E, k, resolve_gather(c) == MK_GATHER_STAGED).total;
+    return ws_layout(T, H, E, k, resolve_gather(c, T, H, E, k) == MK_GATHER_STAGED).total;
 }
 
 }  // extern "C"
@@ -318,11 +326,11 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
         return cudaMemsetAsync(expert_offsets, 0, size_t(E + 1) * 4, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
     }
 
-    const bool direct = resolve_gather(c) == MK_GATHER_DIRECT;
-    const int mma = resolve_pair(c, T, E, k, direct);
+    const bool direct = resolve_gather(c, T, H, E, k) == MK_GATHER_DIRECT;
+    const int mma = resolve_pair(c, T, E, k);
     const bool pair = mma == MK_MMA_PAIR, wide = mma == MK_MMA_WIDE;
     if (pair && W3) return MK_ERR_UNSUPPORTED;  // the gated FFN runs on single-SM tiles
-    if (direct && (pair || wide)) return MK_ERR_UNSUPPORTED;  // 256-row tiles load staged rows only
+    if (direct && pair) return MK_ERR_UNSUPPORTED;  // SM pairs load staged rows only
     // direct rows are addressed with 32-bit byte offsets into x
     if (direct && uint64_t(T) * uint64_t(H) * 2 >= (uint64_t(1) << 32)) return MK_ERR_UNSUPPORTED;
     int grid = grid_for(*d, c);
@@ -470,7 +478,7 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     // one fused launch, staged rows, tiles on one SM (128-row or wide)
     if (c.mode != MK_MODE_FUSED || c.gather == MK_GATHER_DIRECT || c.mma_pair == MK_MMA_PAIR)
         return MK_ERR_UNSUPPORTED;
-    const bool wide = resolve_pair(c, T, E, k, false) == MK_MMA_WIDE;
+    const bool wide = resolve_pair(c, T, E, k) == MK_MMA_WIDE;
     if (!expert_offsets || !aligned(expert_offsets, 4)) return MK_ERR_INVALID_ARG;
     if (T > 0) {
         if (!x || !logits || !W || !y_tok || !src_index || !gate_w) return MK_ERR_INVALID_ARG;

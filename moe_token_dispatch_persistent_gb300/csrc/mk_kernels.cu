@@ -775,8 +775,17 @@ __device__ __forceinline__ void store_row32(const Params& p, size_t row, int col
 // generic-proxy writes before the tensor core's reads with a proxy fence.
 // One warp alone cannot issue the copies as fast as the tensor core consumes
 // them, hence several.
+//
+// WIDE (256-row tiles): each copy warp fills one whole 128-row A block of
+// the stage; a tile of at most 128 rows needs only the first.
+template <bool WIDE>
 __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const CUtensorMap* tmB3, CtrlSmem* cs,
                                 const int cw, const WaitCtx& wp) {
+    static_assert(!WIDE || COPY_WARPS == 2, "wide tiles: one 128-row block per copy warp");
+    constexpr int NST = WIDE ? WSTAGES : STAGES;
+    constexpr int ASB = WIDE ? 2 * A_STAGE_BYTES : A_STAGE_BYTES;
+    constexpr int SMB = NST * ASB;
+    constexpr int ROWS = WIDE ? BM : COPY_ROWS;  // A rows this warp copies per stage
     const int lane = threadIdx.x & 31;
     const bool leader = cw == 0;
     uint8_t* s = smem_base();
@@ -825,10 +834,10 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
         inf.nbk = __shfl_sync(0xffffffffu, inf.nbk, 0);
         // byte offset in x of the tile rows this lane copies (rows past the
         // tile repeat its first row; their products are never stored)
-        uint32_t rowoff[COPY_ROWS / 4];
+        uint32_t rowoff[ROWS / 4];
 #pragma unroll
-        for (int i = 0; i < COPY_ROWS / 4; ++i) {
-            const int r = cw * COPY_ROWS + 4 * i + (lane >> 3);
+        for (int i = 0; i < ROWS / 4; ++i) {
+            const int r = cw * ROWS + 4 * i + (lane >> 3);
             const int q = __ldcg(p.src_index + inf.row0 + (r < inf.nrows ? r : 0));
             rowoff[i] = uint32_t(min(max(q / p.k, 0), p.T - 1)) * uint32_t(p.H) * 2u;
         }
@@ -840,19 +849,19 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
             if (leader) mbar_arrive_expect_tx_elect(&cs->full[stage], B_STAGE_BYTES);
             __syncwarp();  // the expect-tx before this warp's copies arrive
             uint64_t* fb = &cs->full[stage];
-            uint8_t* a = s + SM_A + stage * A_STAGE_BYTES + cw * COPY_ROWS * 128;
-            {
+            uint8_t* a = s + stage * ASB + cw * ROWS * 128;
+            if (!WIDE || cw * ROWS < inf.nrows) {
                 const int c = lane & 7, rq = lane >> 3;
                 const uint8_t* src = reinterpret_cast<const uint8_t*>(p.x) + kb * (BK * 2) + c * 16;
                 const uint32_t d0 = smem_u32(a) + rq * 128 + ((c ^ rq) << 4);             // rows 4i + rq, i even
                 const uint32_t d1 = smem_u32(a) + (4 + rq) * 128 + ((c ^ (4 + rq)) << 4);  // i odd: row % 8 = 4 + rq
 #pragma unroll
-                for (int i = 0; i < COPY_ROWS / 4; ++i)
+                for (int i = 0; i < ROWS / 4; ++i)
                     cp_async_16_u32(((i & 1) ? d1 - 512 : d0) + 512 * i, src + rowoff[i]);
-                cp_async_mbar_arrive_noinc(fb);
             }
+            cp_async_mbar_arrive_noinc(fb);  // fires once this lane's copies (if any) have landed
             if (leader) {
-                uint8_t* b = s + SM_B + stage * B_STAGE_BYTES;
+                uint8_t* b = s + SMB + stage * B_STAGE_BYTES;
                 const int ncol = p.F;
                 if (p.gated) {
 #pragma unroll
@@ -874,7 +883,7 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
                 issued_any |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
             }
-            if (++stage == STAGES) {
+            if (++stage == NST) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -884,7 +893,7 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
     cp_async_wait_all();  // no copy of this warp outlives the role
     if (!ok && leader && lane == 0) {
         WaitCtx shortw{nullptr, 0u, 5000000LL};
-        for (int st = 0; st < STAGES; ++st)
+        for (int st = 0; st < NST; ++st)
             if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
     }
     __syncwarp();
@@ -941,8 +950,8 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     // that times out and is recorded is the one at the root.
     const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
 
-    if (!WIDE && p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
-        producer_direct(p, tmB, tmB3, cs, warp == 0 ? 0 : warp - EPI_WARP_END + 1, wp);
+    if (p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
+        producer_direct<WIDE>(p, tmB, tmB3, cs, warp == 0 ? 0 : warp - EPI_WARP_END + 1, wp);
     } else if (warp == 0) {
         // ---------------- TMA producer: the whole warp runs the loop, one elected lane issues ----------------
         uint32_t stage = 0, phase = 0;
@@ -1763,7 +1772,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (cs->bcast[2]) {
             stamp(p, 6);
             if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, true, flag, w);
-            else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), true, flag, w);
+            else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), !p.direct, flag, w);
             else compute_role<false>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), !p.direct, flag, w);
             stamp(p, 7);
         }

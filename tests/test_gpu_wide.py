@@ -187,13 +187,29 @@ def test_wide_full_size_equals_single(wid):
     assert err <= gu.Y_TOL[mk.MK_OUT_BF16], f"rel-inf {err:.3e}"
 
 
-def test_wide_unsupported_with_direct_rows():
-    T, H, F, E, k = 64, 64, 64, 4, 2
-    xd, ld, Wd = gu.to_device(*_inputs(T, H, F, E, k))
-    o = mk.alloc_outputs(T, F, E, k)
-    st = mk.mk_moe_dispatch_gemm_ex(xd, ld, T, H, E, k, Wd, F, o["y_sorted"], o["src_index"], o["expert_offsets"],
-                                    o["gate_w"], None, mk.make_config(mma_pair=WIDE, gather=mk.MK_GATHER_DIRECT))
-    assert st == mk.MK_ERR_UNSUPPORTED
+@pytest.mark.parametrize("shape", [(700, 256, 256, 8, 2), (300, 192, 128, 4, 3), (1, 64, 64, 1, 1)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_wide_direct_rows_bitwise(shape):
+    """Rows straight from x into wide tiles (each copy warp fills one 128-row
+    block): the same bits as staged 128-row tiles."""
+    T, H, F, E, k = shape
+    x, l, W = gu.to_device(*_inputs(T, H, F, E, k, seed=23 + T))
+    a = gu.run_gpu(x, l, W, k, cfg=mk.make_config(mma_pair=mk.MK_MMA_SINGLE))
+    b = gu.run_gpu(x, l, W, k, cfg=mk.make_config(mma_pair=WIDE, gather=mk.MK_GATHER_DIRECT))
+    info = mk.mk_last_launch_info()
+    assert info["mma_pair"] == WIDE and info["gather"] == mk.MK_GATHER_DIRECT
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_wide_direct_rows_full_size():
+    w = synth.WORKLOADS[2]
+    x, l, W = synth.make_inputs(w)
+    xd, ld, Wd = gu.to_device(x, l, W)
+    a = gu.run_gpu(xd, ld, Wd, w.k, cfg=mk.make_config(mma_pair=mk.MK_MMA_SINGLE))
+    b = gu.run_gpu(xd, ld, Wd, w.k, cfg=mk.make_config(mma_pair=WIDE, gather=mk.MK_GATHER_DIRECT))
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key])
 
 
 @pytest.mark.parametrize("R", [1, 2, 4, 8])
@@ -209,3 +225,19 @@ def test_wide_expert_parallel_bitwise(R):
     assert torch.equal(g["src_index"], single["src_index"])
     assert torch.equal(g["y_tok"][order], single["y_sorted"])
     assert torch.equal(g["out"], single["out"])
+
+
+@pytest.mark.parametrize("T,E,k,tiles,gather", [
+    (4096, 8, 2, WIDE, mk.MK_GATHER_STAGED),          # Mixtral-like shape: wide, staged
+    (2048, 64, 8, WIDE, mk.MK_GATHER_DIRECT),          # fine-grained routing: wide, rows straight from x
+    (128, 256, 8, mk.MK_MMA_SINGLE, mk.MK_GATHER_STAGED),  # decode: 4 rows per expert
+    (1000, 64, 8, mk.MK_MMA_SINGLE, mk.MK_GATHER_STAGED),  # 125 rows per expert on average
+])
+def test_auto_resolution(T, E, k, tiles, gather):
+    """What AUTO picks, per shape (the reported launch facts)."""
+    H, F = 64, 64
+    xd, ld, Wd = gu.to_device(*_inputs(T, H, F, E, k, seed=31))
+    mk.moe_dispatch_gemm(xd, ld, Wd, k)
+    torch.cuda.synchronize()
+    info = mk.mk_last_launch_info()
+    assert info["mma_pair"] == tiles and info["gather"] == gather

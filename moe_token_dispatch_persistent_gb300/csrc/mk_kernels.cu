@@ -19,19 +19,23 @@
 //                           order, rows moved with 1-D bulk copies through
 //                           shared memory, a release flag per finished tile;
 //                           then the CTA joins the compute role
-//   compute role           TMA producer warp -> 4-stage mbarrier ring ->
-//                           tcgen05.mma (128x256x16, fp32 in TMEM, double
-//                           buffered) -> 4 epilogue warps (tcgen05.ld,
+//   compute role           TMA producer warp -> mbarrier ring -> MMA warp
+//                           (tcgen05.mma 128x256x16, fp32 in TMEM; both
+//                           loops run on whole warps, one elected lane
+//                           issues) -> 4 epilogue warps (tcgen05.ld,
 //                           bf16/f32 stores of the tile's valid rows); with
 //                           streamed results each finished chunk of rows
-//                           raises a flag for a copy stream
+//                           raises a flag for a copy stream.  Tiles of 128
+//                           rows (4 stages, double-buffered accumulators) or
+//                           wide tiles of 256 rows (3 stages; two
+//                           accumulators share each weight stage)
 //   phase C  (optional)    after a grid barrier, the weighted sum of each
 //                           token's k rows (the MoE layer's combine)
 //
 // Variants of the same pipeline: the gated FFN (W1 and W3 columns side by
 // side in one N = 256 product, SwiGLU in the epilogue); rows copied straight
-// from x by the producer warps instead of staged by the dispatch role; SM
-// pairs (cta_group::2, 256-row tiles); and mk_ep_kernel, which runs R
+// from x by two copy warps instead of staged by the dispatch role (on 128-row
+// or wide tiles); SM pairs (cta_group::2, 256-row tiles); and mk_ep_kernel, which runs R
 // logical ranks of an expert-parallel layer in one launch.  The same device
 // functions also run as four or five separate launches (route, scan,
 // push-gather, GEMM, combine): the host-driven baseline the fused kernel is

@@ -53,6 +53,11 @@ def parse_args(argv=None):
     ap.add_argument("--n-group", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip unfused / dispatch-only / e2e / cpu legs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--dispatch-only", action="store_true",
+                    help="time the dispatch role alone (routing, scan, gather; no GEMM) as the main loop, in GB/s")
+    ap.add_argument("--experts-div", type=int, default=1,
+                    help="small case for profiler captures: E/D experts and T/D tokens, H, F, k and the value "
+                         "recipe unchanged (not a bench workload)")
     return ap.parse_args(argv)
 
 
@@ -101,6 +106,26 @@ def ncu_traffic(workload_name: str):
     except OSError:
         return None
     return rec["bytes_per_launch"] if digest == rec["kernel_code_sha256"] else None
+
+
+def reduced_workload(w: synth.Workload, d: int) -> synth.Workload:
+    """The same layer with E/d experts and T/d tokens: H, F, k, the seed and
+    the value recipe stay, so the rows per expert stay about the same while
+    the weights shrink d-fold.  A small case of the same kernel for profiler
+    captures of workloads whose full size holds many GB on the device."""
+    if d == 1:
+        return w
+    if d < 1 or w.E % d or w.T % d or w.E // d < 32:
+        raise SystemExit(f"--experts-div {d}: needs a divisor of E={w.E} and T={w.T} leaving at least 32 experts")
+    return synth.Workload(f"{w.name}_experts_div_{d}", w.T // d, w.H, w.F, w.E // d, w.k, w.seed, w.kind)
+
+
+def roofline_bound(w: synth.Workload, active_experts: int, peaks) -> str:
+    """The bound of the fused launch: the larger of the time its FLOPs take
+    at the bf16 peak and the time its compulsory bytes take at the HBM peak."""
+    t_tensor = w.flop / (float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * 1e12)
+    t_hbm = compulsory_bytes(w, active_experts) / (float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])) * 1e9)
+    return "tensor" if t_tensor >= t_hbm else "hbm"
 
 
 def workload_config(w: synth.Workload, extra=None):
@@ -334,7 +359,8 @@ def run_ours(args, w):
     out = mk.alloc_outputs(w.T, w.F, w.E, w.k, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    cfg = mk.make_config(dispatch_ctas=args.dispatch_ctas, n_group=args.n_group)
+    cfg = mk.make_config(dispatch_ctas=args.dispatch_ctas, n_group=args.n_group,
+                         mode=mk.MK_MODE_DISPATCH_ONLY if args.dispatch_only else mk.MK_MODE_FUSED)
 
     combined = torch.empty((w.T, w.F), dtype=torch.bfloat16, device=dev)
 
@@ -392,31 +418,52 @@ def run_ours(args, w):
     offs = out["expert_offsets"].cpu().numpy()
     active = int((np.diff(offs) > 0).sum())
 
-    achieved = w.flop / (ms_mean / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    unit = UNIT
+    if args.dispatch_only:
+        # the dispatch role alone: its algorithmic bytes against HBM
+        db = dispatch_bytes(w)
+        achieved = db / (ms_mean / 1e3) / 1e9
+        value = db * world / (ms_max / 1e3) / 1e9
+        unit = "GB/s"
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"hbm_gbs, {peaks_src}", "kernel": "mk_fused_kernel (dispatch only)",
+                "traffic": None, "algorithmic_bytes": db}
+    elif roofline_bound(w, active, peaks) == "hbm":
+        # weight streaming (few rows per expert): compulsory bytes against HBM
+        cb = compulsory_bytes(w, active)
+        achieved = cb / (ms_mean / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"hbm_gbs, {peaks_src}", "kernel": "mk_fused_kernel",
+                "traffic": ncu_traffic(w.name), "compulsory_bytes": cb,
+                "tflops": w.flop / (ms_mean / 1e3) / 1e12}
+    else:
+        achieved = w.flop / (ms_mean / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"bf16_tflops (burst), {peaks_src}",
+                "kernel": "mk_fused_kernel", "traffic": ncu_traffic(w.name),
+                "compulsory_bytes": compulsory_bytes(w, active)}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, {"mode": "fused persistent", "grid_ctas": info["grid_ctas"],
+        "config": workload_config(w, {"mode": "dispatch only" if args.dispatch_only else "fused persistent",
+                                      "grid_ctas": info["grid_ctas"],
                                       "dispatch_ctas": info["dispatch_ctas"], "n_group": info["n_group"],
                                       "tiles": TILE_NAMES.get(info["mma_pair"], str(info["mma_pair"])),
                                       "active_experts": active}),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": f"bf16_tflops (burst), {peaks_src}",
-                     "kernel": "mk_fused_kernel", "traffic": ncu_traffic(w.name),
-                     "compulsory_bytes": compulsory_bytes(w, active)},
+        "roofline": roof,
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "ms_per_step_min": min(ms), "ms_per_step_median": statistics.median(ms),
     }
 
-    if not args.no_extras:
+    if not (args.no_extras or args.dispatch_only):
         # dispatch role alone (routing + gather), GB/s against HBM
         dcfg = mk.make_config(mode=mk.MK_MODE_DISPATCH_ONLY)
         dms = statistics.mean(timed(dcfg, min(args.steps, 50), 3))
         db = dispatch_bytes(w)
-        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         line["dispatch"] = {"gbs": db / (dms / 1e3) / 1e9, "frac_hbm": db / (dms / 1e3) / 1e9 / hbm,
                             "ms": dms, "bytes": db, "peak_gbs": hbm}
         # the same steps as four launches (host-driven baseline)
@@ -528,7 +575,7 @@ def run_ours(args, w):
 
 def main(argv=None):
     args = parse_args(argv)
-    w = synth.WORKLOADS[args.config]
+    w = reduced_workload(synth.WORKLOADS[args.config], args.experts_div)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

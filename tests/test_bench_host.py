@@ -81,3 +81,31 @@ def test_kernel_code_digest_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.kernel_code_digest(["a.cu"]) == d0
     a.write_text("int f(int x) {\n  return 3 * x;\n}\n")
     assert bench.kernel_code_digest(["a.cu"]) != d0
+
+
+def test_roofline_bound_follows_the_workload():
+    """The Mixtral-like, skewed and imbalanced layers are bound by the bf16
+    peak; the decode layer (a few rows per expert) by streaming its weights."""
+    import numpy as np
+
+    peaks = dict(bench.FALLBACK_PEAKS)
+    for wid, bound in ((2, "tensor"), (3, "tensor"), (5, "tensor"), (4, "hbm")):
+        w = bench.synth.WORKLOADS[wid]
+        # experts that receive rows: only their weights are compulsory bytes
+        top = np.argsort(-bench.synth.make_logits(w), axis=1, kind="stable")[:, :w.k]
+        active = int((np.bincount(top.ravel(), minlength=w.E) > 0).sum())
+        assert bench.roofline_bound(w, active, peaks) == bound, w.name
+    # all 256 experts of the skewed layer active would make it weight-bound
+    assert bench.roofline_bound(bench.synth.WORKLOADS[3], 256, peaks) == "hbm"
+
+
+def test_reduced_workload_keeps_rows_per_expert():
+    w = bench.synth.WORKLOADS[3]
+    r = bench.reduced_workload(w, 8)
+    assert (r.T, r.E) == (w.T // 8, w.E // 8) and (r.H, r.F, r.k, r.seed, r.kind) == (w.H, w.F, w.k, w.seed, w.kind)
+    assert r.rows / r.E == w.rows / w.E and r.name != w.name
+    assert bench.reduced_workload(w, 1) is w
+    import pytest
+
+    with pytest.raises(SystemExit):
+        bench.reduced_workload(bench.synth.WORKLOADS[2], 2)  # 4 experts: too few

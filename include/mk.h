@@ -128,6 +128,8 @@ typedef struct mk_launch_info {
     int64_t workspace_bytes;
     int32_t mma_pair;       /* MK_MMA_SINGLE, MK_MMA_PAIR or MK_MMA_WIDE as resolved */
     int32_t gather;         /* MK_GATHER_STAGED or MK_GATHER_DIRECT as resolved */
+    int32_t route_lanes;    /* lanes sharing each token's experts in routing (1, 2, 4, 8) */
+    int32_t route_chunks;   /* routing chunks (224 / route_lanes tokens each) */
 } mk_launch_info_t;
 
 /* Fill `cfg` with the defaults (fused, bf16 output, heuristic split). */

@@ -98,6 +98,8 @@ class mk_launch_info_t(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("mma_pair", ctypes.c_int32),
         ("gather", ctypes.c_int32),
+        ("route_lanes", ctypes.c_int32),
+        ("route_chunks", ctypes.c_int32),
     ]
 
 

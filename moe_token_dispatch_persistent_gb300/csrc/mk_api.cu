@@ -337,7 +337,9 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     if (pair) grid &= ~1;  // whole clusters of two
     if (grid < (pair ? 2 : 1)) return MK_ERR_UNSUPPORTED;
     const int rows = T * k;
-    const int nch = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    const int route_lanes = route_lanes_for(T, E, grid, aligned(logits, 16));
+    const int route_chunk = ROUTE_CHUNK / route_lanes;
+    const int nch = (T + route_chunk - 1) / route_chunk;
     if (nch > grid * MAX_CHUNKS_PER_CTA) return MK_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, H, E, k, !direct);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -366,6 +368,8 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.y_v8 = aligned(y_sorted, 32) ? 1 : 0;
     p.rows = rows;
     p.nch = nch;
+    p.route_lanes = route_lanes;
+    p.route_chunk = route_chunk;
     p.gated = W3 ? 1 : 0;
     p.W3 = static_cast<const uint16_t*>(W3);
     const int bnw = W3 ? BN / 2 : BN;  // gated: 128 columns of each projection per item
@@ -450,6 +454,8 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     g_last_info.n_group = p.n_group;
     g_last_info.mma_pair = mma;
     g_last_info.gather = direct ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
+    g_last_info.route_lanes = route_lanes;
+    g_last_info.route_chunks = nch;
     g_last_info.workspace_bytes = int64_t(L.total);
     if (getenv("MK_LOG"))
         fprintf(stderr, "[mk] T=%d H=%d F=%d E=%d k=%d mode=%d grid=%d dispatch=%d n_group=%d slots=%d ws=%zu\n", T, H,
@@ -538,6 +544,8 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     p.y_v8 = aligned(y_tok, 32) ? 1 : 0;
     p.rows = T * k;
     p.nch = L.nch;
+    p.route_lanes = 1;  // each rank's chunks keep a lane per token
+    p.route_chunk = ROUTE_CHUNK;
     p.nb = nb;
     p.kblocks = H / BK;
     // ranks stream their own experts' weights at once, so they share L2
@@ -607,6 +615,8 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     g_last_info.n_group = p.n_group;
     g_last_info.mma_pair = wide ? MK_MMA_WIDE : MK_MMA_SINGLE;
     g_last_info.gather = MK_GATHER_STAGED;
+    g_last_info.route_lanes = 1;
+    g_last_info.route_chunks = L.nch;
     g_last_info.workspace_bytes = int64_t(L.total);
     return err == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }

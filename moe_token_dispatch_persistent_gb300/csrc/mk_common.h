@@ -28,6 +28,7 @@ constexpr int COPY_ROWS = BM / COPY_WARPS;            // A rows per copy warp an
 static_assert(COPY_ROWS % 8 == 0, "each copy warp owns whole 8-row swizzle atoms");
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int ROUTE_CHUNK = NWARPS * 32;              // tokens per routing chunk (lane per token)
+constexpr int MAX_ROUTE_LANES = 8;                    // lanes sharing one token's experts (E >= 64)
 constexpr int MAX_E = 256;
 constexpr int MAX_K = 8;
 constexpr int MAX_CHUNKS_PER_CTA = 16;
@@ -65,9 +66,13 @@ constexpr int RT_LOGITS_BYTES = NWARPS * 32 * RT_LOGIT_STRIDE * 4;
 constexpr int RT_IDX = RT_LOGITS + RT_LOGITS_BYTES;
 constexpr int RT_LRANK = RT_IDX + NWARPS * 32 * MAX_K * 4;
 constexpr int RT_WCNT = RT_LRANK + NWARPS * 32 * MAX_K * 4;
-constexpr int RT_BASES = RT_WCNT + NWARPS * MAX_E * 4;
-constexpr int RT_END = RT_BASES + MAX_CHUNKS_PER_CTA * MAX_E * 4;
-static_assert(RT_END <= SM_STAGE_END, "routing scratch must fit in the stage area");
+constexpr int RT_WCNT_END = RT_WCNT + NWARPS * MAX_E * 4;
+// The bases of a CTA's own chunks sit at the end of the stage area: the
+// scan copies the whole count table to [0, RT_BASES) once the routing
+// scratch is dead, so up to RT_BASES / 4 counts are scanned in shared memory.
+constexpr int RT_BASES = SM_STAGE_END - MAX_CHUNKS_PER_CTA * MAX_E * 4;
+static_assert(RT_WCNT_END <= RT_BASES, "routing scratch must fit below the chunk bases");
+static_assert(RT_BASES / 4 >= 152 * MAX_E, "one chunk per SM of every expert's counts fits in shared memory");
 static_assert(SM_PB + PSTAGES * PB_STAGE_BYTES <= SM_STAGE_END, "pair stages must fit in the stage area");
 
 // Control block at the head of the workspace.  The kernels leave it ready
@@ -147,6 +152,8 @@ struct Params {
     // derived sizes
     int rows;                // T*k
     int nch;                 // routing chunks
+    int route_lanes;         // lanes sharing each token's experts in routing: 1, 2, 4 or 8
+    int route_chunk;         // tokens per routing chunk: ROUTE_CHUNK / route_lanes
     int nb;                  // N-blocks per expert, ceil(F / BN)
     int kblocks;             // H / BK
     int n_group;             // N-blocks per group in the work order
@@ -213,10 +220,37 @@ inline size_t ws_align(size_t v) { return (v + 255) & ~size_t(255); }
 
 constexpr int MAX_GRID = 1024;
 
+// Lanes per token for routing.  With E = 64, 128 or 256 experts a token's
+// experts are split over S lanes (S * 32 or S * 64 experts, read with
+// 16-byte loads), so a chunk holds ROUTE_CHUNK / S tokens and S times as
+// many CTAs route.  S is the largest split whose chunks still number at
+// most one per CTA and whose count table (chunks x E) stays within 20480
+// counts: every CTA scans the whole table, and on GB300 a 147 x 256 table
+// cost more scan time than the split saved in routing.  S = 1 (a lane per
+// token) for other expert counts, for logits that are not 16-byte aligned,
+// or when no split passes both limits.
+inline int route_lanes_for(int T, int E, int grid, bool logits_16b) {
+    if (!logits_16b) return 1;
+    int S = E == 64 ? 2 : E == 128 ? 4 : E == 256 ? MAX_ROUTE_LANES : 1;
+    while (S > 1 && (int64_t(T) + ROUTE_CHUNK / S - 1) / (ROUTE_CHUNK / S) > grid) S >>= 1;
+    // the scan reads every chunk's counts: at most 20480 of them (80 KiB)
+    while (S > 1 && (int64_t(T) + ROUTE_CHUNK / S - 1) / (ROUTE_CHUNK / S) * E > 20480) S >>= 1;
+    if (S > 1 && E / S > 64) S = 1;  // a lane scans 32 or 64 experts
+    return S;
+}
+
+// Routing chunks of a call: with S > 1 there are at most `grid` of them.
+inline size_t route_chunks_bound(int T) {
+    const size_t whole = (size_t(T) + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    const size_t split = (size_t(T) + ROUTE_CHUNK / MAX_ROUTE_LANES - 1) / (ROUTE_CHUNK / MAX_ROUTE_LANES);
+    const size_t capped = split < size_t(MAX_GRID) ? split : size_t(MAX_GRID);
+    return whole > capped ? whole : capped;
+}
+
 inline WsLayout ws_layout(int T, int H, int E, int k, bool staging = true, int grid = MAX_GRID) {
     WsLayout L{};
     const size_t rows = size_t(T) * k;
-    const size_t nch = (size_t(T) + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    const size_t nch = route_chunks_bound(T);
     const size_t max_tiles = (rows + BM - 1) / BM + E;
     size_t o = 0;
     L.ctl = o;        o = ws_align(o + sizeof(Ctl));

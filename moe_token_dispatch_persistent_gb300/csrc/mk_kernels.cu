@@ -9,8 +9,10 @@
 // para. 2).  On one GPU the "communication" role is the gather of token rows
 // from x into expert-contiguous tiles in HBM:
 //
-//   phase R  (all CTAs)    router top-k + gates per token (lane per token),
-//                           per-chunk histogram and stable in-chunk ranks
+//   phase R  (all CTAs)    router top-k + gates per token (a lane per token,
+//                           or 2-8 lanes sharing a token's experts when
+//                           E = 64, 128, 256), per-chunk histogram and
+//                           stable in-chunk ranks
 //   barrier               every chunk's counts are in
 //   phase S  (all CTAs)    per-expert totals, exclusive scan -> offsets,
 //                           tile and work-item tables (each CTA, in smem);
@@ -199,25 +201,210 @@ __device__ __forceinline__ CtrlSmem* ctrl() { return reinterpret_cast<CtrlSmem*>
 // ------------------------------------------------------------ phase R ------
 
 // Tokens [t0, t1) of routing chunk c: rank r's tokens [ep_t0[r], ep_t0[r+1])
-// are cut into chunks of ROUTE_CHUNK from the rank's first token (one rank:
-// chunk c covers [c*ROUTE_CHUNK, ...)).  Chunks in id order cover the tokens
-// in order, so the sorted order does not depend on where chunks begin.
+// are cut into chunks of route_chunk tokens from the rank's first token (one
+// rank: chunk c covers [c*route_chunk, ...)).  Chunks in id order cover the
+// tokens in order, so the sorted order does not depend on where chunks begin.
 __device__ __forceinline__ void chunk_tokens(const Params& p, int c, int& t0, int& t1) {
     int r = 0;
     while (r + 1 < p.ranks && p.ep_c0[r + 1] <= c) ++r;
-    t0 = p.ep_t0[r] + (c - p.ep_c0[r]) * ROUTE_CHUNK;
-    t1 = min(t0 + ROUTE_CHUNK, p.ep_t0[r + 1]);
+    t0 = p.ep_t0[r] + (c - p.ep_c0[r]) * p.route_chunk;
+    t1 = min(t0 + p.route_chunk, p.ep_t0[r + 1]);
 }
 
 // Key order of the router: (value desc, expert id asc).
 __device__ __forceinline__ bool beats(float v, int e, float u, int f) { return v > u || (v == u && e < f); }
 
-// Route one chunk of ROUTE_CHUNK tokens: top-k + gates, per-chunk histogram,
-// and each (t, j)'s rank among the chunk's entries of the same expert in
-// (t, j) order.  Whole CTA.  The chunk's count row goes to the count table,
-// or, simulating expert parallelism, to every rank's copy of it (the
-// all-gather of the counts).
-__device__ void route_chunk(const Params& p, int c) {
+// Sorted insertion of (v, e) into a best-first list of MAX_K entries.
+__device__ __forceinline__ void topk_insert(float v, int e, float (&vals)[MAX_K], int (&ids)[MAX_K]) {
+    if (beats(v, e, vals[MAX_K - 1], ids[MAX_K - 1])) {
+        bool b[MAX_K];
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) b[j] = beats(v, e, vals[j], ids[j]);
+#pragma unroll
+        for (int j = MAX_K - 1; j >= 0; --j) {
+            if (b[j]) {
+                const bool prev = (j > 0) && b[j - 1];
+                vals[j] = prev ? vals[j - 1] : v;
+                ids[j] = prev ? ids[j - 1] : e;
+            }
+        }
+    }
+}
+
+// Keep the best MAX_K of this lane's list and that of lane ^ d (both
+// best-first, from disjoint experts): entry j against the partner's entry
+// MAX_K-1-j gives the best MAX_K as a bitonic sequence, which three
+// compare-exchange rounds sort.  Both lanes end with the same list.
+__device__ __forceinline__ void topk_merge_xor(int d, float (&vals)[MAX_K], int (&ids)[MAX_K]) {
+    float pv[MAX_K];
+    int pi[MAX_K];
+#pragma unroll
+    for (int j = 0; j < MAX_K; ++j) {
+        pv[j] = __shfl_xor_sync(0xffffffffu, vals[j], d);
+        pi[j] = __shfl_xor_sync(0xffffffffu, ids[j], d);
+    }
+#pragma unroll
+    for (int j = 0; j < MAX_K; ++j) {
+        if (beats(pv[MAX_K - 1 - j], pi[MAX_K - 1 - j], vals[j], ids[j])) {
+            vals[j] = pv[MAX_K - 1 - j];
+            ids[j] = pi[MAX_K - 1 - j];
+        }
+    }
+#pragma unroll
+    for (int h = MAX_K / 2; h > 0; h >>= 1) {
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
+            if ((j & h) == 0 && beats(vals[j + h], ids[j + h], vals[j], ids[j])) {
+                const float tv = vals[j];
+                const int ti = ids[j];
+                vals[j] = vals[j + h];
+                ids[j] = ids[j + h];
+                vals[j + h] = tv;
+                ids[j + h] = ti;
+            }
+        }
+    }
+}
+
+// Route one chunk with S = p.route_lanes > 1 lanes sharing each token
+// (E = S * NPL, NPL = 32 or 64; a warp routes 32/S tokens, a chunk
+// NWARPS*32/S).  The warp's 32/S logits rows are one contiguous block of
+// 32 * NPL floats, read with 16-byte loads and laid out in shared memory as
+// 32 segments of NPL (+1 pad) floats, segment (token g, part s) at lane
+// g * S + s.  Each lane keeps the best MAX_K of its NPL experts, and log2(S)
+// merges give every lane of the token the best MAX_K of all E.  The best
+// MAX_K under the key (value desc, id asc) is unique, so the lists equal
+// those of a lane per token.  One copy of the code serves every S (runtime).
+__device__ void route_chunk_split(const Params& p, int c) {
+    uint8_t* s = smem_base();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.route_lanes, E = p.E, k = p.k;
+    const int lgS = __ffs(S) - 1;
+    const int TPW = 32 >> lgS;     // tokens per warp
+    const int NPL = E >> lgS;      // experts per lane: 32 or 64
+    const int NV = NPL >> 2;       // 16-byte loads per lane: 8 or 16
+    float* slog = reinterpret_cast<float*>(s + RT_LOGITS) + warp * 32 * RT_LOGIT_STRIDE;
+    int* sidx = reinterpret_cast<int*>(s + RT_IDX) + warp * 32 * MAX_K;
+    int* slr = reinterpret_cast<int*>(s + RT_LRANK) + warp * 32 * MAX_K;
+    int* wcnt = reinterpret_cast<int*>(s + RT_WCNT);
+    int tc0, T;  // the chunk's tokens [tc0, T)
+    chunk_tokens(p, c, tc0, T);
+    const int tbase = tc0 + warp * TPW;
+    const int g = lane >> lgS, sub = lane & (S - 1);  // token of the lane in the warp, part of its experts
+    const int t = tbase + g;
+
+    for (int e = lane; e < E; e += 32) wcnt[warp * MAX_E + e] = 0;
+
+    const int nvalid = max(0, min(TPW, T - tbase)) * S * NV;  // float4s of the warp's valid rows
+    const float4* blk = reinterpret_cast<const float4*>(p.logits + size_t(tbase) * E);
+    float4 q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int f = i * 32 + lane;
+        q[i] = (i < NV && f < nvalid) ? __ldg(blk + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        if (i < NV) {
+            const int f = (i * 32 + lane) * 4;  // first float of the load in the warp's block
+            float* d = slog + (f / NPL) * (NPL + 1) + f % NPL;
+            d[0] = q[i].x;
+            d[1] = q[i].y;
+            d[2] = q[i].z;
+            d[3] = q[i].w;
+        }
+    }
+    __syncwarp();
+
+    float vals[MAX_K];
+    int ids[MAX_K];
+#pragma unroll
+    for (int j = 0; j < MAX_K; ++j) {
+        vals[j] = -INFINITY;
+        ids[j] = 0x7fffffff;
+    }
+    if (t < T) {
+        const float* seg = slog + lane * (NPL + 1);
+        const int e0 = sub * NPL;
+#pragma unroll 4
+        for (int i = 0; i < NPL; ++i) topk_insert(seg[i], e0 + i, vals, ids);
+    }
+    for (int d = 1; d < S; d <<= 1) topk_merge_xor(d, vals, ids);
+
+    if (sub == 0 && t < T) {
+        // ids outside [0, E) only survive for NaN rows (outside the contract)
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) ids[j] = min(max(ids[j], 0), E - 1);
+        const float l0 = vals[0];
+        float gv[MAX_K];
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
+            gv[j] = 0.f;
+            if (j < k && l0 != -INFINITY) {
+                gv[j] = expf(vals[j] - l0);
+                sum += gv[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
+            if (j < k) {
+                const float gj = (l0 == -INFINITY) ? 0.f : gv[j] / sum;
+                p.topk_idx[size_t(t) * k + j] = ids[j];
+                p.topk_gate[size_t(t) * k + j] = gj;
+                sidx[g * MAX_K + j] = ids[j];
+            }
+        }
+    }
+    __syncwarp();
+
+    // In-warp stable ranks over the warp's TPW tokens, 32/k per pass.
+    const int G = 32 / k;
+    const uint32_t lt = lanemask_lt();
+    for (int it = 0; it * G < TPW; ++it) {
+        const int gg = lane / k, j = lane - (lane / k) * k;
+        const int tok = it * G + gg;
+        const bool valid = (lane < G * k) && (tok < TPW) && (tbase + tok < T);
+        const int e = valid ? sidx[tok * MAX_K + j] : -(lane + 1);
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        const int before = __popc(peers & lt);
+        const int base = valid ? wcnt[warp * MAX_E + e] : 0;
+        __syncwarp();
+        if (valid && before == 0) wcnt[warp * MAX_E + e] = base + __popc(peers);
+        __syncwarp();
+        if (valid) slr[tok * MAX_K + j] = base + before;
+    }
+    __syncthreads();
+
+    // Chunk counts and per-warp exclusive bases.
+    for (int e = threadIdx.x; e < E; e += NTHREADS) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) {
+            const int v = wcnt[w * MAX_E + e];
+            wcnt[w * MAX_E + e] = run;
+            run += v;
+        }
+        p.counts[size_t(c) * E + e] = run;
+    }
+    __syncthreads();
+    if (lane < TPW && tbase + lane < T) {
+        const int tt = tbase + lane;
+        for (int j = 0; j < k; ++j) {
+            const int e = sidx[lane * MAX_K + j];
+            p.lrank[size_t(tt) * k + j] = slr[lane * MAX_K + j] + wcnt[warp * MAX_E + e];
+        }
+    }
+    __syncthreads();
+}
+
+// Route one chunk of ROUTE_CHUNK tokens, a lane per token: top-k + gates,
+// per-chunk histogram, and each (t, j)'s rank among the chunk's entries of
+// the same expert in (t, j) order.  Whole CTA.  The chunk's count row goes
+// to the count table, or, simulating expert parallelism, to every rank's
+// copy of it (the all-gather of the counts).
+__device__ void route_chunk_lane(const Params& p, int c) {
     uint8_t* s = smem_base();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* slog = reinterpret_cast<float*>(s + RT_LOGITS) + warp * 32 * RT_LOGIT_STRIDE;
@@ -352,6 +539,15 @@ __device__ void route_chunk(const Params& p, int c) {
     __syncthreads();
 }
 
+// The routing form the host chose (route_lanes_for).  Measured on GB300:
+// each extra copy of the routing code in this kernel slowed the lane-per-
+// token path by up to 2 µs, so the split form is one runtime-generic copy
+// and the lane path comes first.
+__device__ void route_chunk(const Params& p, int c) {
+    if (p.route_lanes <= 1) route_chunk_lane(p, c);
+    else route_chunk_split(p, c);
+}
+
 // ------------------------------------------------------------ phase S ------
 
 // Exclusive scans of per-expert totals into offsets, tile starts and item
@@ -416,20 +612,16 @@ __device__ void scan_counts(const Params& p, CtrlSmem* cs, const int32_t* counts
     const int total = nch * E;
     const bool in_smem = total <= RT_BASES / 4;
     if (in_smem) {
-        // copy the counts table to shared memory, 8 independent loads per thread in flight
-        for (int b0 = 0; b0 < total; b0 += NTHREADS * 8) {
-            int v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = b0 + j * NTHREADS + threadIdx.x;
-                v[j] = i < total ? __ldcg(counts + i) : 0;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = b0 + j * NTHREADS + threadIdx.x;
-                if (i < total) scnt[i] = v[j];
-            }
-        }
+        // copy the counts table to shared memory with 16-byte cp.async (L2
+        // only: the rows come from other CTAs), all of a thread's copies in
+        // flight at once.  The last piece may read up to 12 bytes of the
+        // table's padding (its workspace region is 256-byte aligned and
+        // sized), which nothing uses.
+        const int n16 = (total + 3) / 4;
+        const uint32_t dst = smem_u32(scnt);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(counts);
+        for (int i = threadIdx.x; i < n16; i += NTHREADS) cp_async_16_u32(dst + uint32_t(i) * 16u, src + size_t(i) * 16);
+        cp_async_wait_all();
         __syncthreads();
     }
     const int s_lo = src_rank >= 0 ? p.ep_c0[src_rank] : 0;

@@ -55,7 +55,7 @@ def test_config_defaults(lib):
 
 def test_struct_layouts_match_header(lib):
     assert ctypes.sizeof(mk.mk_config_t) == 64
-    assert ctypes.sizeof(mk.mk_launch_info_t) == 32
+    assert ctypes.sizeof(mk.mk_launch_info_t) == 40
 
 
 @pytest.mark.parametrize("T,H,E,k,F,want", [

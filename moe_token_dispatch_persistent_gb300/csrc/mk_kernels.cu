@@ -275,6 +275,8 @@ __device__ __forceinline__ void topk_merge_xor(int d, float (&vals)[MAX_K], int 
 // merges give every lane of the token the best MAX_K of all E.  The best
 // MAX_K under the key (value desc, id asc) is unique, so the lists equal
 // those of a lane per token.  One copy of the code serves every S (runtime).
+// Single-device launches only: the expert-parallel kernel routes with a lane
+// per token, so the count row goes to the one count table.
 __device__ void route_chunk_split(const Params& p, int c) {
     uint8_t* s = smem_base();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -446,6 +448,7 @@ __device__ void route_chunk_lane(const Params& p, int c) {
         }
         __syncwarp();
         if (t < T) {
+            // the sorted insertion of topk_insert, written out in place
 #pragma unroll 4
             for (int ee = 0; ee < ne; ++ee) {
                 const float v = slog[lane * RT_LOGIT_STRIDE + ee];

@@ -109,3 +109,16 @@ def test_reduced_workload_keeps_rows_per_expert():
 
     with pytest.raises(SystemExit):
         bench.reduced_workload(bench.synth.WORKLOADS[2], 2)  # 4 experts: too few
+
+
+def test_reference_arm_on_a_reduced_case():
+    """`--experts-div` names the reduced layer in the line's config."""
+    import json
+
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "3",
+                          "--experts-div", "8", "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                         timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    d = json.loads([ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")][0])
+    assert d["config"]["workload"].startswith("fine_grained_skewed_experts_div_8(T=1024,H=7168,F=2048,E=32,k=8")
+    assert d["config"]["E"] == 32 and d["config"]["T"] == 1024 and d["value"] > 0

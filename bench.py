@@ -3,22 +3,29 @@
 
 One step = one pass of the whole path (router top-k, histogram + scan,
 gather into expert-contiguous tiles, expert GEMM) over one batch of the
-seeded synthetic workload, through the C ABI.  Default workload: the
-Mixtral-like layer (T=4096, H=4096, F=14336, E=8, top-2, seed 1).
+seeded synthetic workload, through the C ABI.  The headline workload is the
+Mixtral-like layer (T=4096, H=4096, F=14336, E=8, top-2, seed 1); at one GPU
+the same JSON line also carries a ``per_config`` block that measures all
+five seeded workloads (tiny, Mixtral-like, fine-grained skewed, decode,
+imbalanced large batch) the same way: fused and unfused launches, the
+dispatch role alone, the roofline of the workload's bound, the clocks seen
+during its timed region, and the CPU oracle on a bounded sample of it.
 
-Timing: W warm-up steps, then K timed steps; every step is bracketed by CUDA
-events on the launching stream, with a 256 MiB write (larger than L2)
-between steps outside the events; the timed region is bracketed by a
-barrier and a device synchronise; the max over ranks is taken.  Under
-torchrun every rank runs its own batch (weak scaling, no data-path
-collective).
+Timing: W warm-up steps, then exactly K timed steps; every step is bracketed
+by CUDA events on the launching stream, with a 256 MiB write (larger than
+L2) between steps outside the events; the timed region is bracketed by a
+barrier and a device synchronise; the max over ranks is taken.  Clocks and
+throttle reasons are sampled in-process through NVML queries every 0.5 ms
+while the timed region runs.  Under torchrun every rank runs its own batch
+(weak scaling, no data-path collective).
 
-``--impl reference`` times the CPU oracle instead (rank 0 only).
-Prints ONE JSON line on rank 0.
+``--impl reference`` times the CPU oracle instead (rank 0 only), each step a
+bounded sample of the same workload.  Prints ONE JSON line on rank 0.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import datetime
 import json
 import os
@@ -26,6 +33,7 @@ import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 import numpy as np
@@ -39,20 +47,27 @@ from moe_token_dispatch_persistent_gb300 import synth  # noqa: E402
 METRIC = "fused dispatch+grouped-GEMM TFLOP/s (% bf16 peak) and dispatch GB/s (% HBM)"
 UNIT = "TFLOP/s"
 FLUSH_BYTES = 256 << 20
+L2_NOTE = "flushed between timed GPU steps (256 MiB write, outside the events)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--config", type=int, default=2, choices=sorted(synth.WORKLOADS),
+                    help="headline workload (the line's value)")
+    ap.add_argument("--configs", default="1,2,3,4,5",
+                    help="workloads of the per_config block at one GPU (comma list, or 'none')")
     ap.add_argument("--dispatch-ctas", type=int, default=0)
     ap.add_argument("--n-group", type=int, default=0)
-    ap.add_argument("--no-extras", action="store_true", help="skip unfused / dispatch-only / e2e / cpu legs")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline only: no per_config block and no unfused / dispatch-only / e2e / cpu legs")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the headline CPU-baseline sample")
+    ap.add_argument("--cpu-seconds-per-config", type=float, default=4.0,
+                    help="budget of each per_config CPU-baseline sample")
     ap.add_argument("--dispatch-only", action="store_true",
                     help="time the dispatch role alone (routing, scan, gather; no GEMM) as the main loop, in GB/s")
     ap.add_argument("--experts-div", type=int, default=1,
@@ -92,20 +107,26 @@ def kernel_code_digest(paths) -> str:
 
 def ncu_traffic(workload_name: str):
     """DRAM bytes (read + write) per launch of the fused kernel from the
-    committed ncu capture of this workload, or None when there is none or the
-    kernel code changed since it was taken."""
+    committed ncu capture of this workload (profiles/ncu_traffic.json), or
+    None when there is none or the kernel code changed since it was taken.
+    Returns (bytes, source) or (None, reason)."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             rec = json.load(f).get(workload_name)
     except (OSError, ValueError):
-        return None
+        return None, "no committed capture"
     if not rec:
-        return None
+        return None, "no committed capture of this workload"
     try:
         digest = kernel_code_digest(rec["kernel_sources"])
     except OSError:
-        return None
-    return rec["bytes_per_launch"] if digest == rec["kernel_code_sha256"] else None
+        return None, "kernel sources missing"
+    if digest != rec["kernel_code_sha256"]:
+        return None, "kernel code changed since the committed capture"
+    src = f"committed ncu capture ({rec.get('source', 'profiles/')}), kernel code digest matches"
+    if rec.get("scaled_from"):
+        src += f"; {rec['scaled_from']}"
+    return rec["bytes_per_launch"], src
 
 
 def reduced_workload(w: synth.Workload, d: int) -> synth.Workload:
@@ -120,6 +141,18 @@ def reduced_workload(w: synth.Workload, d: int) -> synth.Workload:
     return synth.Workload(f"{w.name}_experts_div_{d}", w.T // d, w.H, w.F, w.E // d, w.k, w.seed, w.kind)
 
 
+def compulsory_bytes(w: synth.Workload, active_experts: int) -> int:
+    """x + logits + active experts' W + y_sorted (bf16) + src_index + gate_w + offsets."""
+    return (w.T * w.H * 2 + w.T * w.E * 4 + active_experts * w.H * w.F * 2 + w.rows * w.F * 2 + w.rows * 8
+            + (w.E + 1) * 4)
+
+
+def dispatch_bytes(w: synth.Workload) -> int:
+    """Algorithmic bytes of the dispatch role: logits read, token rows read and
+    written to the staging tiles, src_index / gate_w written, offsets."""
+    return w.T * w.E * 4 + 2 * w.rows * w.H * 2 + w.rows * 8 + (w.E + 1) * 4
+
+
 def roofline_bound(w: synth.Workload, active_experts: int, peaks) -> str:
     """The bound of the fused launch: the larger of the time its FLOPs take
     at the bf16 peak and the time its compulsory bytes take at the HBM peak."""
@@ -128,12 +161,11 @@ def roofline_bound(w: synth.Workload, active_experts: int, peaks) -> str:
     return "tensor" if t_tensor >= t_hbm else "hbm"
 
 
-def workload_config(w: synth.Workload, extra=None):
-    c = {"workload": w.describe(), "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k, "seed": w.seed,
-         "l2": "flushed between timed steps (256 MiB write, outside the events)"}
-    if extra:
-        c.update(extra)
-    return c
+def bench_config(w: synth.Workload):
+    """The line's ``config``: the workload and how L2 is handled.  Both arms
+    print exactly this dict, so the two lines name the same workload."""
+    return {"workload": w.describe(), "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k, "seed": w.seed,
+            "l2": L2_NOTE}
 
 
 def dist_env():
@@ -160,72 +192,189 @@ def whole_job_tflops(flop_per_rank: float, world: int, seconds_max: float) -> fl
     return flop_per_rank * world / seconds_max / 1e12
 
 
-class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+# ---------------------------------------------------------------- clocks --
+
+# NVML clocks-event reason bits (nvml.h): the four the timing rules name.
+_REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                "hw_thermal_slowdown": 0x40}
+_NVML_CLOCK_SM = 1
+
+
+class NvmlClocks:
+    """SM clock and throttle reasons of one GPU, sampled in-process every
+    ``period_s`` by a thread doing NVML queries (read only) while a timed
+    region runs, so that short regions still hold samples.  ``start_region``
+    starts the thread, ``end_region`` stops it; ``region()`` summarises the
+    samples of the last region (with the one the caller takes from the main
+    thread by ``sample_now`` while the GPU still runs the enqueued steps)."""
+
+    def __init__(self, nvml_index: int, period_s: float = 0.0005):
+        self.ok = False
+        self.period = period_s
+        self.samples = []  # (t, sm_mhz, reasons_bits)
+        self.lock = threading.Lock()
+        self.t0 = self.t1 = None
+        self._stop = threading.Event()
+        self._th = None
+        try:
+            lib = None
+            for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+                try:
+                    lib = ctypes.CDLL(name)
+                    break
+                except OSError:
+                    continue
+            if lib is None or lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(nvml_index), ctypes.byref(h)) != 0:
+                return
+            self.lib, self.h = lib, h
+            mx = ctypes.c_uint()
+            self.max_mhz = (float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, _NVML_CLOCK_SM, ctypes.byref(mx)) == 0
+                            else None)
+            self._reasons_fn = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                                or getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+            self.ok = self.read() is not None
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def read(self):
+        mhz = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, _NVML_CLOCK_SM, ctypes.byref(mhz)) != 0:
+            return None
+        bits = ctypes.c_ulonglong(0)
+        if self._reasons_fn is not None:
+            self._reasons_fn(self.h, ctypes.byref(bits))
+        return (time.perf_counter(), float(mhz.value), int(bits.value))
+
+    def _loop(self):
+        while not self._stop.is_set():
+            s = self.read()
+            if s is not None:
+                with self.lock:
+                    self.samples.append(s)
+            time.sleep(self.period)
+
+    def sample_now(self):
+        if self.ok:
+            s = self.read()
+            if s is not None:
+                with self.lock:
+                    self.samples.append(s)
+
+    def start_region(self):
+        with self.lock:
+            self.samples = []
+        self.t0 = time.perf_counter()
+        if self.ok:
+            self._stop.clear()
+            self._th = threading.Thread(target=self._loop, daemon=True)
+            self._th.start()
+
+    def end_region(self):
+        self.t1 = time.perf_counter()
+        if self._th is not None:
+            self._stop.set()
+            self._th.join(timeout=2)
+            self._th = None
+
+    def stop(self):
+        pass
+
+    def region(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0,
+                    "samples_in_timed_region": 0, "source": "none"}
+        with self.lock:
+            inside = [s for s in self.samples if self.t0 <= s[0] <= self.t1]
+        reasons = sorted({nm for s in inside for nm, b in _REASON_BITS.items() if s[2] & b})
+        mhz = [s[1] for s in inside]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_mhz_min": min(mhz) if mhz else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(inside),
+                "samples_in_timed_region": len(inside), "period_ms": self.period * 1e3,
+                "timed_region_ms": (self.t1 - self.t0) * 1e3, "source": "nvml queries in-process"}
+
+
+class SmiClocks:
+    """Fallback when NVML cannot be loaded: nvidia-smi sampling every 50 ms
+    for the whole run (queries only); a region keeps the rows inside it."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+        self.gpu, self.proc = gpu_index, None
         self.t0 = self.t1 = None
-
-    def start(self):
-        """Start sampling; returns once the first sample is written (or after 5 s)."""
+        self.ok = True
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu), "-lms", str(self.PERIOD_MS)], stdout=self.fh,
+                                          "-i", str(self.gpu), "-lms", "50"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-            return
-        deadline = time.time() + 5.0
-        while time.time() < deadline and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
-            time.sleep(0.02)
 
-    def mark_start(self):
+    def sample_now(self):
+        pass
+
+    def start_region(self):
         self.t0 = time.time()
 
-    def mark_end(self):
+    def end_region(self):
         self.t1 = time.time()
+        time.sleep(0.06)  # the sample after the region is written
 
     def stop(self):
-        """Median SM clock and the throttle reasons of the samples taken between
-        mark_start and mark_end (all samples if none fell inside)."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                try:
-                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
-                except ValueError:
-                    continue
         os.unlink(self.path)
-        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
-        use = inside or rows
+        self.proc = None
+
+    def region(self):
+        rows = []
+        if self.proc is not None:
+            self.fh.flush()
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                    except ValueError:
+                        continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({nm for r in use for nm, v in zip(names, r[3]) if v.lower().startswith("active")})
-        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
-                "sm_max_mhz": max(r[2] for r in use) if use else None, "reasons": reasons,
-                "samples": len(use), "samples_in_timed_region": len(inside), "period_ms": self.PERIOD_MS}
+        reasons = sorted({nm for r in inside for nm, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None, "reasons": reasons,
+                "samples": len(inside), "samples_in_timed_region": len(inside), "period_ms": 50,
+                "source": "nvidia-smi"}
+
+
+def make_clock_sampler(local: int):
+    try:
+        import torch
+
+        idx = torch.cuda._get_nvml_device_index(local)
+    except Exception:  # noqa: BLE001 -- any failure: the plain index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = int(vis.split(",")[local]) if vis and vis.split(",")[local].strip().isdigit() else local
+    s = NvmlClocks(idx)
+    if s.ok:
+        return s
+    return SmiClocks(idx)
 
 
 # ------------------------------------------------------------ reference --
@@ -236,10 +385,12 @@ _WE_CACHE = {}
 def oracle_sample(w: synth.Workload, budget_s: float, inputs=None):
     """Time the CPU oracle on a bounded sample of workload ``w``.
 
-    The full routing + dispatch of all T tokens is timed once; the fp64
-    expert product is timed on a sample of sorted rows sized to the budget.
-    The full-workload time is estimated as t_routing + t_row * T*k, and the
-    value is the workload's FLOPs over that estimate.
+    One sample = the routing + dispatch of all T tokens plus the fp64 expert
+    product of n sorted rows of the most loaded expert, n sized so the
+    product takes about ``budget_s``.  The value is the sample's product
+    FLOPs (2*n*H*F; routing counts no FLOPs) over the sample's wall time, a
+    measured rate; the time the whole workload would take at that rate is
+    reported beside it, marked as an estimate.
     """
     from oracle.oracle import Oracle
 
@@ -271,16 +422,19 @@ def oracle_sample(w: synth.Workload, budget_s: float, inputs=None):
     t0 = time.perf_counter()
     orc.expert_rows(x, We[None], w.k, off1, src1, np.arange(n))
     t_rows = time.perf_counter() - t0
-    t_row = t_rows / n
-    est = t_route + t_row * w.rows
+    t_step = t_route + t_rows
+    flop = 2.0 * n * w.H * w.F
+    rate = flop / t_step
     return {
-        "value": w.flop / est / 1e12,
+        "value": rate / 1e12,
         "unit": UNIT,
         "cores": orc.num_threads(),
         "kind": "oracle",
-        "sample": (f"routing+dispatch of all {w.T} tokens ({t_route:.3f} s) + fp64 product of {n} sorted rows "
-                   f"({t_rows:.2f} s); full-workload time estimated as t_route + t_row*{w.rows} = {est:.1f} s"),
-        "seconds_estimated_full": est,
+        "sample": (f"routing+dispatch of all {w.T} tokens ({t_route:.3f} s) + fp64 product of {n} of {w.rows} "
+                   f"sorted rows ({t_rows:.2f} s); value = the sample's product FLOPs / its time"),
+        "sample_seconds": t_step,
+        "full_workload_seconds_estimated": w.flop / rate,
+        "estimated": True,
     }
 
 
@@ -288,23 +442,27 @@ def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    per_step_budget = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
-    times, cb = [], None
+    # each step a bounded sample: the whole run ends within a few minutes
+    per_step_budget = max(0.05, min(4.0, 100.0 / max(1, args.steps + args.warmup)))
+    times, rates, cb = [], [], None
     ch = synth._streams(w)
     inputs = (synth.make_x(w, ch), synth.make_logits(w, ch))
     for i in range(args.warmup + args.steps):
         r = oracle_sample(w, per_step_budget, inputs)
         if i >= args.warmup:
-            times.append(r["seconds_estimated_full"])
+            times.append(r["sample_seconds"])
+            rates.append(r["value"])
             cb = r
-    est = statistics.mean(times)
-    value = w.flop / est / 1e12
+    value = statistics.mean(rates)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": workload_config(w, {"l2": "n/a (CPU)"}),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"]},
+        "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": bench_config(w),
+        "step": "one bounded sample of the workload on the host cores (see cpu_baseline.sample)",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"],
+                         "full_workload_seconds_estimated": cb["full_workload_seconds_estimated"],
+                         "estimated": True},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -314,26 +472,146 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------ ours --
 
-def dispatch_bytes(w: synth.Workload) -> int:
-    """Algorithmic bytes of the dispatch role: logits read, token rows read and
-    written to the staging tiles, src_index / gate_w written, offsets."""
-    return w.T * w.E * 4 + 2 * w.rows * w.H * 2 + w.rows * 8 + (w.E + 1) * 4
-
-
 TILE_NAMES = {1: "128-row", 2: "256-row on SM pairs", 3: "256-row (two accumulators per SM)"}
+GATHER_NAMES = {1: "staged rows", 2: "rows straight from x"}
 
 
-def compulsory_bytes(w: synth.Workload, active_experts: int) -> int:
-    """x + logits + active experts' W + y_sorted (bf16) + src_index + gate_w + offsets."""
-    return (w.T * w.H * 2 + w.T * w.E * 4 + active_experts * w.H * w.F * 2 + w.rows * w.F * 2 + w.rows * 8
-            + (w.E + 1) * 4)
+class Gpu:
+    """Device state of one rank: the library, the stream, the L2 flush buffer."""
+
+    def __init__(self, local: int):
+        import torch
+
+        import moe_token_dispatch_persistent_gb300 as mk
+        from moe_token_dispatch_persistent_gb300 import build
+
+        self.torch, self.mk = torch, mk
+        build.build()
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=self.dev)
+
+    def upload(self, x_np, l_np, W_np):
+        torch = self.torch
+        x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(self.dev)
+        logits = torch.from_numpy(l_np).to(self.dev)
+        W = torch.from_numpy(W_np.view(np.int16)).view(torch.bfloat16).to(self.dev)
+        return x, logits, W
+
+    def timed(self, call, steps, warmup, clocks=None):
+        """Per-step CUDA-event times (ms) of ``call``; with ``clocks`` the
+        timed region is marked on the sampler."""
+        torch, mk = self.torch, self.mk
+        for _ in range(warmup):
+            self.flush.fill_(1)
+            call()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if clocks is not None:
+            clocks.start_region()
+        for a, b in evs:
+            self.flush.fill_(1)
+            a.record(self.stream)
+            call()
+            b.record(self.stream)
+        if clocks is not None:
+            clocks.sample_now()  # the GPU is still running the enqueued steps
+        torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.end_region()
+        st = mk.mk_get_status(self.stream)
+        if st != mk.MK_OK:
+            raise mk.MkError(st, "device status")
+        return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline(w, active, ms_mean, peaks, peaks_src):
+    """Roofline of the fused launch on workload ``w`` (its bound chosen by
+    roofline_bound), from the mean CUDA-event time of a launch."""
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    traffic, tsrc = ncu_traffic(w.name)
+    cb = compulsory_bytes(w, active)
+    if roofline_bound(w, active, peaks) == "hbm":
+        achieved = cb / (ms_mean / 1e3) / 1e9
+        r = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+             "peak_source": f"hbm_gbs (copy: read+write bytes), {peaks_src}",
+             "note": "mostly reads: a read stream can exceed the copy bandwidth, so frac can pass 1",
+             "tflops": w.flop / (ms_mean / 1e3) / 1e12}
+    else:
+        achieved = w.flop / (ms_mean / 1e3) / 1e12
+        r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+             "peak_source": f"bf16_tflops (burst), {peaks_src}"}
+    r.update({"kernel": "mk_fused_kernel", "traffic": traffic, "traffic_source": tsrc, "compulsory_bytes": cb,
+              "algorithmic_per_launch": w.flop if r["bound"] == "tensor" else cb})
+    return r
+
+
+def measure_workload(g: Gpu, w: synth.Workload, args, peaks, peaks_src, clocks, inputs=None, cpu_budget=4.0,
+                     headline_ms=None):
+    """One workload of the per_config block: fused launch (K steps), the same
+    steps as four launches, the dispatch role alone, roofline, clocks and the
+    CPU oracle on a bounded sample."""
+    mk, torch = g.mk, g.torch
+    ch = synth._streams(w)
+    if inputs is None:
+        x_np, l_np = synth.make_x(w, ch), synth.make_logits(w, ch)
+        W_np = synth.make_w(w)
+        x, logits, W = g.upload(x_np, l_np, W_np)
+        del W_np
+    else:
+        x_np, l_np, x, logits, W = inputs
+    out = mk.alloc_outputs(w.T, w.F, w.E, w.k, device=g.dev)
+
+    def call(c):
+        st = mk.mk_moe_dispatch_gemm_ex(x, logits, w.T, w.H, w.E, w.k, W, w.F, out["y_sorted"], out["src_index"],
+                                        out["expert_offsets"], out["gate_w"], g.stream, c)
+        if st != mk.MK_OK:
+            raise mk.MkError(st, "mk_moe_dispatch_gemm_ex")
+
+    cfg = mk.make_config()
+    if headline_ms is None:
+        ms = g.timed(lambda: call(cfg), args.steps, args.warmup, clocks)
+        clk = clocks.region()
+    else:
+        ms, clk = headline_ms
+    info = mk.mk_last_launch_info() if headline_ms is None else None
+    if info is None:
+        call(cfg)
+        torch.cuda.synchronize()
+        info = mk.mk_last_launch_info()
+    active = int((np.diff(out["expert_offsets"].cpu().numpy()) > 0).sum())
+    ms_mean = statistics.mean(ms)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ucfg = mk.make_config(mode=mk.MK_MODE_UNFUSED)
+    ums = statistics.mean(g.timed(lambda: call(ucfg), args.steps, 3))
+    dcfg = mk.make_config(mode=mk.MK_MODE_DISPATCH_ONLY)
+    dms = statistics.mean(g.timed(lambda: call(dcfg), args.steps, 3))
+    db = dispatch_bytes(w)
+    rec = {
+        "workload": w.describe(),
+        "ms_mean": ms_mean, "ms_median": statistics.median(ms), "ms_min": min(ms), "steps": len(ms),
+        "tflops": w.flop / (ms_mean / 1e3) / 1e12,
+        "roofline": roofline(w, active, ms_mean, peaks, peaks_src),
+        "clocks": clk,
+        "fused_ms": ms_mean, "unfused_ms": ums, "fused_speedup": ums / ms_mean, "unfused_launches_per_step": 4,
+        "dispatch": {"gbs": db / (dms / 1e3) / 1e9, "frac_hbm": db / (dms / 1e3) / 1e9 / hbm, "ms": dms,
+                     "bytes": db, "peak_gbs": hbm, "peak_source": f"hbm_gbs, {peaks_src}"},
+        "active_experts": active,
+        "launch": {"grid_ctas": info["grid_ctas"], "dispatch_ctas": info["dispatch_ctas"],
+                   "n_group": info["n_group"], "tiles": TILE_NAMES.get(info["mma_pair"], str(info["mma_pair"])),
+                   "rows": GATHER_NAMES.get(info["gather"], str(info["gather"])),
+                   "route_lanes": info["route_lanes"]},
+    }
+    if cpu_budget > 0:
+        rec["cpu_baseline"] = {k: v for k, v in oracle_sample(w, cpu_budget, (x_np, l_np)).items()
+                               if k != "sample_seconds"}
+    del out
+    return rec
 
 
 def run_ours(args, w):
     import torch
-
-    import moe_token_dispatch_persistent_gb300 as mk
-    from moe_token_dispatch_persistent_gb300 import build
 
     world, rank, local = dist_env()
     if world > 1:
@@ -343,26 +621,23 @@ def run_ours(args, w):
         dist.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
-    build.build()
-    dev = torch.device("cuda", torch.cuda.current_device())
+    g = Gpu(local)
+    mk = g.mk
     peaks, peaks_src = load_peaks()
+    clocks = make_clock_sampler(local)
 
     # inputs: each rank its own batch of tokens (seed offset), same expert weights
     wr = synth.Workload(w.name, w.T, w.H, w.F, w.E, w.k, w.seed + 1000 * rank, w.kind) if rank else w
     ch = synth._streams(wr)
     x_np, l_np = synth.make_x(wr, ch), synth.make_logits(wr, ch)
     W_np = synth.make_w(w)
-    x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(dev)
-    logits = torch.from_numpy(l_np).to(dev)
-    W = torch.from_numpy(W_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    x, logits, W = g.upload(x_np, l_np, W_np)
     del W_np
-    out = mk.alloc_outputs(w.T, w.F, w.E, w.k, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    out = mk.alloc_outputs(w.T, w.F, w.E, w.k, device=g.dev)
+    stream = g.stream
     cfg = mk.make_config(dispatch_ctas=args.dispatch_ctas, n_group=args.n_group,
                          mode=mk.MK_MODE_DISPATCH_ONLY if args.dispatch_only else mk.MK_MODE_FUSED)
-
-    combined = torch.empty((w.T, w.F), dtype=torch.bfloat16, device=dev)
+    combined = torch.empty((w.T, w.F), dtype=torch.bfloat16, device=g.dev)
 
     def call(c, combine=False):
         if combine:
@@ -375,48 +650,24 @@ def run_ours(args, w):
         if st != mk.MK_OK:
             raise mk.MkError(st, "mk_moe_dispatch_gemm_ex")
 
-    def timed(c, steps, warmup, combine=False):
-        for _ in range(warmup):
-            flush.fill_(1)
-            call(c, combine)
-        torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for a, b in evs:
-            flush.fill_(1)
-            a.record(stream)
-            call(c, combine)
-            b.record(stream)
-        torch.cuda.synchronize()
-        st = mk.mk_get_status(stream)
-        if st != mk.MK_OK:
-            raise mk.MkError(st, "device status")
-        return [a.elapsed_time(b) for a, b in evs]
-
-    # headline: fused path
-    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local])
-                           if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
+    # headline: the fused path, exactly K timed steps
     for _ in range(args.warmup):
-        flush.fill_(1)
+        g.flush.fill_(1)
         call(cfg)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler.start()
-    launches_before = 0
-    sampler.mark_start()
-    ms = timed(cfg, args.steps, 0)
+    ms = g.timed(lambda: call(cfg), args.steps, 0, clocks)
     torch.cuda.synchronize()
-    sampler.mark_end()
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop()
+    clk = clocks.region()
     info = mk.mk_last_launch_info()
-    gpu_launches = args.steps * info["launches"] + launches_before
+    gpu_launches = args.steps * info["launches"]
     ms_mean = statistics.mean(ms)
     ms_max = reduce_max(ms_mean, world)
     value = whole_job_tflops(w.flop, world, ms_max / 1e3)
-    offs = out["expert_offsets"].cpu().numpy()
-    active = int((np.diff(offs) > 0).sum())
+    active = int((np.diff(out["expert_offsets"].cpu().numpy()) > 0).sum())
 
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -429,58 +680,47 @@ def run_ours(args, w):
         unit = "GB/s"
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "peak_source": f"hbm_gbs, {peaks_src}", "kernel": "mk_fused_kernel (dispatch only)",
-                "traffic": None, "algorithmic_bytes": db}
-    elif roofline_bound(w, active, peaks) == "hbm":
-        # weight streaming (few rows per expert): compulsory bytes against HBM
-        cb = compulsory_bytes(w, active)
-        achieved = cb / (ms_mean / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "peak_source": f"hbm_gbs, {peaks_src}", "kernel": "mk_fused_kernel",
-                "traffic": ncu_traffic(w.name), "compulsory_bytes": cb,
-                "tflops": w.flop / (ms_mean / 1e3) / 1e12}
+                "traffic": None, "traffic_source": "not captured for this mode", "algorithmic_bytes": db}
     else:
-        achieved = w.flop / (ms_mean / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": f"bf16_tflops (burst), {peaks_src}",
-                "kernel": "mk_fused_kernel", "traffic": ncu_traffic(w.name),
-                "compulsory_bytes": compulsory_bytes(w, active)}
+        roof = roofline(w, active, ms_mean, peaks, peaks_src)
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, {"mode": "dispatch only" if args.dispatch_only else "fused persistent",
-                                      "grid_ctas": info["grid_ctas"],
-                                      "dispatch_ctas": info["dispatch_ctas"], "n_group": info["n_group"],
-                                      "tiles": TILE_NAMES.get(info["mma_pair"], str(info["mma_pair"])),
-                                      "active_experts": active}),
+        "config": bench_config(w),
+        "launch": {"mode": "dispatch only" if args.dispatch_only else "fused persistent",
+                   "grid_ctas": info["grid_ctas"], "dispatch_ctas": info["dispatch_ctas"],
+                   "n_group": info["n_group"], "tiles": TILE_NAMES.get(info["mma_pair"], str(info["mma_pair"])),
+                   "rows": GATHER_NAMES.get(info["gather"], str(info["gather"])), "active_experts": active},
         "roofline": roof,
         "gpu_launches": gpu_launches,
-        "clocks": clocks,
+        "clocks": clk,
         "ms_per_step_min": min(ms), "ms_per_step_median": statistics.median(ms),
     }
 
     if not (args.no_extras or args.dispatch_only):
+        steps_x = min(args.steps, 50)
         # dispatch role alone (routing + gather), GB/s against HBM
         dcfg = mk.make_config(mode=mk.MK_MODE_DISPATCH_ONLY)
-        dms = statistics.mean(timed(dcfg, min(args.steps, 50), 3))
+        dms = statistics.mean(g.timed(lambda: call(dcfg), steps_x, 3))
         db = dispatch_bytes(w)
         line["dispatch"] = {"gbs": db / (dms / 1e3) / 1e9, "frac_hbm": db / (dms / 1e3) / 1e9 / hbm,
                             "ms": dms, "bytes": db, "peak_gbs": hbm}
         # the same steps as four launches (host-driven baseline)
         ucfg = mk.make_config(mode=mk.MK_MODE_UNFUSED)
-        ums = statistics.mean(timed(ucfg, min(args.steps, 50), 3))
+        ums = statistics.mean(g.timed(lambda: call(ucfg), steps_x, 3))
         line["unfused"] = {"ms_per_step": ums, "tflops": w.flop / (ums / 1e3) / 1e12,
                            "fused_speedup": ums / ms_mean, "launches_per_step": 4}
         # the MoE layer's combine (gated sum of each token's expert rows)
-        cms = statistics.mean(timed(cfg, min(args.steps, 50), 3, combine=True))
-        cums = statistics.mean(timed(ucfg, min(args.steps, 50), 3, combine=True))
+        cms = statistics.mean(g.timed(lambda: call(cfg, True), steps_x, 3))
+        cums = statistics.mean(g.timed(lambda: call(ucfg, True), steps_x, 3))
         cbytes = w.rows * w.F * 2 + w.T * w.F * 2 + w.rows * 8  # y_sorted read, out written, rows + gates
         line["combine"] = {"fused_ms": cms, "unfused_ms": cums, "fused_speedup": cums / cms,
                            "added_ms": cms - ms_mean, "bytes": cbytes,
                            "added_gbs": cbytes / max(cms - ms_mean, 1e-6) * 1e3 / 1e9}
         # the gated (SwiGLU) expert FFN: two projections, one tensor-core pass per item
         w3 = synth.Workload(w.name, w.T, w.H, w.F, w.E, w.k, w.seed + 7, w.kind)
-        W3 = torch.from_numpy(synth.make_w(w3).view(np.int16)).view(torch.bfloat16).to(dev)
+        W3 = torch.from_numpy(synth.make_w(w3).view(np.int16)).view(torch.bfloat16).to(g.dev)
 
         def gated_once():
             st = mk.mk_moe_dispatch_gated(x, logits, w.T, w.H, w.E, w.k, W, W3, w.F, out["y_sorted"],
@@ -488,27 +728,13 @@ def run_ours(args, w):
             if st != mk.MK_OK:
                 raise mk.MkError(st, "mk_moe_dispatch_gated")
 
-        for _ in range(3):
-            flush.fill_(1)
-            gated_once()
-        gms_list = []
-        for _ in range(min(args.steps, 50)):
-            flush.fill_(1)
-            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_ev.record(stream)
-            gated_once()
-            b_ev.record(stream)
-            gms_list.append((a_ev, b_ev))
-        torch.cuda.synchronize()
-        if mk.mk_get_status(stream) != mk.MK_OK:
-            raise RuntimeError("gated path: device error")
-        gms = statistics.mean(a.elapsed_time(b) for a, b in gms_list)
+        gms = statistics.mean(g.timed(gated_once, steps_x, 3))
         line["gated"] = {"ms": gms, "tflops": 2 * w.flop / (gms / 1e3) / 1e12,
                          "frac_bf16": 2 * w.flop / (gms / 1e3) / 1e12 / peak}
         del W3
         # token rows straight from x (no staging rows): the same product
         dgcfg = mk.make_config(dispatch_ctas=args.dispatch_ctas, n_group=args.n_group, gather=mk.MK_GATHER_DIRECT)
-        dgms = statistics.mean(timed(dgcfg, min(args.steps, 50), 3))
+        dgms = statistics.mean(g.timed(lambda: call(dgcfg), steps_x, 3))
         line["direct_gather"] = {
             "ms": dgms, "tflops": w.flop / (dgms / 1e3) / 1e12, "frac_bf16": w.flop / (dgms / 1e3) / 1e12 / peak,
             "vs_staged": ms_mean / dgms,
@@ -516,25 +742,14 @@ def run_ours(args, w):
             "staged_workspace_bytes": mk.mk_workspace_size(w.T, w.H, w.F, w.E, w.k, cfg)}
         # expert parallelism simulated on this GPU: the most ranks (<= 8) that divide E
         ranks = max(r for r in (1, 2, 4, 8) if w.E % r == 0)
-        ep_once = lambda c: mk.mk_moe_ep_sim(x, logits, w.T, w.H, w.E, w.k, W, w.F, ranks, out["y_sorted"],  # noqa: E731
-                                             out["src_index"], out["expert_offsets"], out["gate_w"], combined,
-                                             stream, c)
-        for _ in range(3):
-            flush.fill_(1)
-            if ep_once(cfg) != mk.MK_OK:
-                raise RuntimeError("mk_moe_ep_sim refused the configuration")
-        ep_evs = []
-        for _ in range(min(args.steps, 50)):
-            flush.fill_(1)
-            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_ev.record(stream)
-            ep_once(cfg)
-            b_ev.record(stream)
-            ep_evs.append((a_ev, b_ev))
-        torch.cuda.synchronize()
-        if mk.mk_get_status(stream) != mk.MK_OK:
-            raise RuntimeError("expert-parallel path: device error")
-        ems = statistics.mean(a.elapsed_time(b) for a, b in ep_evs)
+
+        def ep_once():
+            st = mk.mk_moe_ep_sim(x, logits, w.T, w.H, w.E, w.k, W, w.F, ranks, out["y_sorted"], out["src_index"],
+                                  out["expert_offsets"], out["gate_w"], combined, stream, cfg)
+            if st != mk.MK_OK:
+                raise mk.MkError(st, "mk_moe_ep_sim")
+
+        ems = statistics.mean(g.timed(ep_once, steps_x, 3))
         line["ep_sim"] = {"ranks": ranks, "ms": ems, "tflops": w.flop / (ems / 1e3) / 1e12,
                           "vs_single_device_with_combine": cms / ems,
                           "workspace_bytes": mk.mk_ep_workspace_size(w.T, w.H, w.F, w.E, w.k, ranks)}
@@ -549,7 +764,7 @@ def run_ours(args, w):
         e2e_steps = max(3, min(args.steps, 30))
         et = []
         for i in range(args.warmup + e2e_steps):
-            flush.fill_(1)
+            g.flush.fill_(1)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             st = mk.mk_moe_dispatch_gemm_host(xh, lh, w.T, w.H, w.E, w.k, W, w.F, yh, sh, oh, gh, stream, cfg)
@@ -563,9 +778,30 @@ def run_ours(args, w):
                        "h2d_bytes_per_step": x_np.nbytes + l_np.nbytes,
                        "d2h_bytes_per_step": yh.numel() * 2 + sh.numel() * 4 + oh.numel() * 4 + gh.numel() * 4,
                        "ms_per_step": e2e_s * 1e3, "api": "mk_moe_dispatch_gemm_host (pinned host buffers)"}
+        del xh, lh, yh, sh, oh, gh
         if rank == 0 and world == 1:
             line["cpu_baseline"] = {k: v for k, v in oracle_sample(w, args.cpu_seconds, (x_np, l_np)).items()
-                                    if k != "seconds_estimated_full"}
+                                    if k != "sample_seconds"}
+        # every workload, one at a time (one GPU only: under torchrun each rank
+        # would repeat the whole set)
+        wanted = [] if args.configs.strip().lower() == "none" else [int(c) for c in args.configs.split(",") if c]
+        if world == 1 and args.experts_div == 1 and wanted:
+            per = {}
+            for cid in wanted:
+                wc = synth.WORKLOADS[cid]
+                if cid == args.config:
+                    rec = measure_workload(g, wc, args, peaks, peaks_src, clocks, (x_np, l_np, x, logits, W),
+                                           cpu_budget=0.0, headline_ms=(ms, clk))
+                    rec["cpu_baseline"] = line["cpu_baseline"]
+                    rec["headline"] = True
+                else:
+                    rec = measure_workload(g, wc, args, peaks, peaks_src, clocks,
+                                           cpu_budget=args.cpu_seconds_per_config)
+                    mk.mk_release_workspace()
+                    torch.cuda.empty_cache()
+                per[wc.describe()] = rec
+            line["per_config"] = per
+    clocks.stop()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -269,11 +269,16 @@ mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_ho
  * nothing (it fits decode-sized batches: about T*k*H*2 bytes of staged rows
  * plus small tables).  No cudaMalloc, cudaFree or allocating library call
  * is made.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call on a device shares the array and
- * finds the previous call's contents there (the call clears what must start
- * at zero), so calls that overlap on the GPU -- on different streams, or
- * from different threads -- race: serialise them. */
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture.  After a device reset
+ * (cudaDeviceReset), call mk_release_workspace() before the next call: it
+ * drops the kept addresses (the array may sit elsewhere in the new context)
+ * as well as the workspace cache.  Every call on a device shares the array
+ * and finds the previous call's contents there (the call clears what must
+ * start at zero), so calls that overlap on the GPU -- on different streams,
+ * or from different threads -- race: serialise them.  cfg->trace must be 0
+ * (MK_ERR_UNSUPPORTED otherwise): phase stamps would land in the array,
+ * where mk_read_trace cannot reach them. */
 mk_status_t mk_moe_dispatch_gemm_noalloc(const void* x, const float* logits, int T, int H, int E, int k,
                                          const void* W, int F, void* y_sorted, int32_t* src_index,
                                          int32_t* expert_offsets, float* gate_w, void* stream,
@@ -301,7 +306,8 @@ void mk_last_launch_info(mk_launch_info_t* info);
 mk_status_t mk_read_trace(void* stream, const void* workspace, int T, int H, int E, int k, uint64_t* out,
                           size_t n);
 
-/* Free the library's workspace cache on every device (synchronises). */
+/* Free the library's workspace cache on every device (synchronises), and
+ * forget the device addresses mk_moe_dispatch_gemm_noalloc looked up. */
 void mk_release_workspace(void);
 
 /* Static string for a status code. */

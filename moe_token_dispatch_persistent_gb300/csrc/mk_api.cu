@@ -32,6 +32,7 @@ cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& 
 cudaError_t set_kernel_attributes();
 cudaError_t fused_max_blocks_per_sm(int* n);
 cudaError_t read_and_clear_error(uint32_t out[4], cudaStream_t st);
+void noalloc_forget_scratch();
 }  // namespace mk
 
 using namespace mk;
@@ -830,6 +831,7 @@ mk_status_t mk_read_trace(void* stream, const void* workspace, int T, int H, int
 }
 
 void mk_release_workspace(void) {
+    noalloc_forget_scratch();  // the allocation-free entry point looks its array up again
     std::lock_guard<std::mutex> lock(g_mu);
     int cur = 0;
     cudaGetDevice(&cur);

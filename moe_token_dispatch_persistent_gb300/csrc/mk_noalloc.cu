@@ -12,6 +12,12 @@
 // GPU on which it is set up keeps it until the process exits (with eager
 // module loading, every GPU that loads the library does).  It is shared by
 // every call on that GPU and keeps the last call's contents.
+//
+// The array's device address is looked up once per device, with that device
+// current, and kept.  A device reset gives the device a new context in which
+// the array may sit elsewhere, so mk_release_workspace() -- which a caller
+// runs after a reset, as it must for the workspace cache too -- forgets the
+// kept addresses and the next call looks them up again.
 
 #include <cuda_runtime.h>
 
@@ -47,10 +53,21 @@ mk_status_t scratch_on_current_device(void** out) {
 
 }  // namespace
 
+namespace mk {
+// Called by mk_release_workspace(): drop every kept device address.
+void noalloc_forget_scratch() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < kMaxDevices; ++i) g_scratch_ptr[i] = nullptr;
+}
+}  // namespace mk
+
 extern "C" mk_status_t mk_moe_dispatch_gemm_noalloc(const void* x, const float* logits, int T, int H, int E, int k,
                                                     const void* W, int F, void* y_sorted, int32_t* src_index,
                                                     int32_t* expert_offsets, float* gate_w, void* stream,
                                                     const mk_config_t* cfg) {
+    // Phase stamps would land in the array, where mk_read_trace cannot find
+    // them: tracing is refused rather than silently lost.
+    if (cfg && cfg->trace != 0) return MK_ERR_UNSUPPORTED;
     // Sizes the fixed array cannot hold are refused before anything runs.
     const size_t need = mk_workspace_size(T, H, F, E, k, cfg);
     if (need > size_t(MK_NOALLOC_SCRATCH_BYTES)) return MK_ERR_WORKSPACE;

@@ -1,5 +1,6 @@
-"""Host logic of bench.py that needs no GPU: the clock sampler keeps only the
-samples taken inside the timed region."""
+"""Host logic of bench.py that needs no GPU: the clock samplers keep only the
+samples taken inside the timed region, the reference arm prints the contract's
+line with the same config as ours, and the roofline picks the workload's bound."""
 import datetime
 import os
 import subprocess
@@ -17,40 +18,78 @@ def _line(ts, sm, reasons=("Not Active",) * 4):
     return ", ".join([stamp, "0", str(sm), "2070", "900.00", "0x0", *reasons]) + "\n"
 
 
-def _sampler_with(lines, t0, t1):
-    s = bench.ClockSampler(0)
+def _smi_with(lines, t0, t1):
+    """An nvidia-smi sampler whose output file already holds ``lines``."""
+    s = bench.SmiClocks.__new__(bench.SmiClocks)
     fd, s.path = tempfile.mkstemp(suffix=".csv")
     os.close(fd)
     with open(s.path, "w") as f:
         f.writelines(lines)
     s.fh = open(os.devnull, "w")
-    s.proc = subprocess.Popen([sys.executable, "-c", "import time; time.sleep(30)"])
-    s.t0, s.t1 = t0, t1
+    s.proc = object()  # stands for the running nvidia-smi
+    s.t0, s.t1, s.ok = t0, t1, True
     return s
 
 
-def test_samples_outside_the_timed_region_are_dropped():
+def test_smi_samples_outside_the_timed_region_are_dropped():
     t0 = 1_800_000_000.0
     lines = [_line(t0 - 1.0, 345, ("Not Active", "Not Active", "Not Active", "Active")),  # idle, before
              _line(t0 + 0.1, 2070), _line(t0 + 0.2, 2055),
              _line(t0 + 0.3, 2040, ("Not Active", "Not Active", "Not Active", "Active")),
              _line(t0 + 5.0, 600, ("Active", "Not Active", "Not Active", "Not Active"))]  # after
-    c = _sampler_with(lines, t0, t0 + 1.0).stop()
+    c = _smi_with(lines, t0, t0 + 1.0).region()
     assert c["samples_in_timed_region"] == 3 and c["samples"] == 3
     assert c["sm_mhz"] == 2055 and c["sm_max_mhz"] == 2070
     assert c["reasons"] == ["sw_power_cap"]  # the hw_slowdown after the region is not counted
 
 
-def test_all_samples_used_when_none_fell_inside():
+def test_smi_region_without_samples_reports_none():
     t0 = 1_800_000_000.0
-    c = _sampler_with([_line(t0 - 2.0, 1900), _line(t0 - 1.0, 2000)], t0, t0 + 0.001).stop()
-    assert c["samples_in_timed_region"] == 0 and c["samples"] == 2 and c["sm_mhz"] == 1950
+    c = _smi_with([_line(t0 - 2.0, 1900), _line(t0 - 1.0, 2000)], t0, t0 + 0.001).region()
+    assert c["samples_in_timed_region"] == 0 and c["sm_mhz"] is None
 
 
-def test_malformed_lines_are_skipped():
+def test_smi_malformed_lines_are_skipped():
     t0 = 1_800_000_000.0
-    c = _sampler_with(["garbage\n", "[N/A], 0\n", _line(t0 + 0.5, 2070)], t0, t0 + 1.0).stop()
+    c = _smi_with(["garbage\n", "[N/A], 0\n", _line(t0 + 0.5, 2070)], t0, t0 + 1.0).region()
     assert c["samples"] == 1 and c["sm_mhz"] == 2070
+
+
+def _nvml_with(samples, t0, t1):
+    import threading
+
+    s = bench.NvmlClocks.__new__(bench.NvmlClocks)
+    s.ok, s.lock, s.samples, s.t0, s.t1, s.max_mhz, s.period = True, threading.Lock(), samples, t0, t1, 2070.0, 5e-4
+    return s
+
+
+def test_nvml_region_keeps_its_samples_and_decodes_reasons():
+    """Reason bits follow nvml.h: 0x4 sw power cap, 0x8 hw slowdown, 0x20 sw
+    thermal, 0x40 hw thermal; other bits (idle 0x1) are not throttling."""
+    t0 = 100.0
+    smp = [(99.0, 400.0, 0x1), (100.001, 2070.0, 0x0), (100.002, 1980.0, 0x4), (100.003, 2040.0, 0x0),
+           (100.5, 900.0, 0x8 | 0x40)]
+    c = _nvml_with(smp, t0, t0 + 0.01).region()
+    assert c["samples_in_timed_region"] == 3 and c["sm_mhz"] == 2040.0 and c["sm_mhz_min"] == 1980.0
+    assert c["reasons"] == ["sw_power_cap"] and c["sm_max_mhz"] == 2070.0
+    c = _nvml_with(smp, 100.4, 100.6).region()
+    assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_nvml_unavailable_is_reported():
+    s = bench.NvmlClocks.__new__(bench.NvmlClocks)
+    s.ok = False
+    c = s.region()
+    assert c["samples_in_timed_region"] == 0 and c["reasons"] == ["nvml unavailable"]
+
+
+def test_both_arms_print_the_same_config():
+    """The reference arm and ours build ``config`` with the same function, so
+    the two lines carry the same keys and values for the same workload."""
+    w = bench.synth.WORKLOADS[2]
+    c = bench.bench_config(w)
+    assert set(c) == {"workload", "T", "H", "F", "E", "k", "seed", "l2"}
+    assert c["workload"] == w.describe() and "flush" in c["l2"]
 
 
 def test_reference_arm_prints_one_json_line():
@@ -69,7 +108,10 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"] and d["e2e"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
-    assert d["config"]["workload"].startswith("tiny")
+    assert d["config"] == bench.bench_config(bench.synth.WORKLOADS[1])
+    # ms_per_step is the measured time of a step (a bounded sample), not an extrapolation
+    assert 0 < d["ms_per_step"] < 600e3
+    assert d["cpu_baseline"]["estimated"] is True and d["cpu_baseline"]["full_workload_seconds_estimated"] > 0
 
 
 def test_kernel_code_digest_ignores_comments_only(tmp_path, monkeypatch):

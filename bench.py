@@ -473,7 +473,7 @@ def run_reference(args, w):
 # ------------------------------------------------------------------ ours --
 
 TILE_NAMES = {1: "128-row", 2: "256-row on SM pairs", 3: "256-row (two accumulators per SM)"}
-GATHER_NAMES = {1: "staged rows", 2: "rows straight from x"}
+GATHER_NAMES = {1: "staged rows", 2: "rows straight from x (cp.async)", 3: "rows straight from x (TMA gather4)"}
 
 
 class Gpu:
@@ -588,6 +588,12 @@ def measure_workload(g: Gpu, w: synth.Workload, args, peaks, peaks_src, clocks, 
     dcfg = mk.make_config(mode=mk.MK_MODE_DISPATCH_ONLY)
     dms = statistics.mean(g.timed(lambda: call(dcfg), args.steps, 3))
     db = dispatch_bytes(w)
+    # the three ways token rows reach the GEMM, on the default tiles
+    forms = {}
+    for name, gv in (("staged", mk.MK_GATHER_STAGED), ("cp_async", mk.MK_GATHER_DIRECT),
+                     ("tma_gather4", mk.MK_GATHER_GATHER4)):
+        fc = mk.make_config(gather=gv)
+        forms[name] = statistics.mean(g.timed(lambda: call(fc), args.steps, 3))
     rec = {
         "workload": w.describe(),
         "ms_mean": ms_mean, "ms_median": statistics.median(ms), "ms_min": min(ms), "steps": len(ms),
@@ -598,6 +604,7 @@ def measure_workload(g: Gpu, w: synth.Workload, args, peaks, peaks_src, clocks, 
         "dispatch": {"gbs": db / (dms / 1e3) / 1e9, "frac_hbm": db / (dms / 1e3) / 1e9 / hbm, "ms": dms,
                      "bytes": db, "peak_gbs": hbm, "peak_source": f"hbm_gbs, {peaks_src}"},
         "active_experts": active,
+        "row_forms_ms": forms,
         "launch": {"grid_ctas": info["grid_ctas"], "dispatch_ctas": info["dispatch_ctas"],
                    "n_group": info["n_group"], "tiles": TILE_NAMES.get(info["mma_pair"], str(info["mma_pair"])),
                    "rows": GATHER_NAMES.get(info["gather"], str(info["gather"])),

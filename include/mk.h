@@ -102,10 +102,14 @@ typedef struct mk_config {
  * producer warp copies each tile's rows straight from x into its
  * shared-memory stages (16-byte cp.async), so there is no staging copy, no
  * gather role, and the workspace holds no staging rows (T*k*H*2 bytes
- * less); 128-row or wide tiles (not SM pairs), and T*H*2 < 4 GiB.  AUTO:
- * DIRECT when k >= 4 and T*k >= 256*E (wide tiles), with cfg.mma_pair AUTO
- * or WIDE and T*H*2 < 4 GiB; STAGED otherwise. */
-enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
+ * less); 128-row or wide tiles (not SM pairs), and T*H*2 < 4 GiB.  GATHER4:
+ * as DIRECT, but the rows arrive by TMA tile::gather4 (four token rows per
+ * instruction, one instruction per lane of the producer warp) instead of
+ * cp.async; same tiles and limits.  AUTO: DIRECT when k >= 4 and
+ * T*k >= 256*E (wide tiles), with cfg.mma_pair AUTO or WIDE and
+ * T*H*2 < 4 GiB; STAGED otherwise.  The expert-parallel entry points stage
+ * rows (DIRECT and GATHER4 return MK_ERR_UNSUPPORTED there). */
+enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2, MK_GATHER_GATHER4 = 3 };
 
 /* Expert GEMM tile.  SINGLE: each CTA runs a 128 x 256 tile alone.  PAIR: a
  * cluster of two CTAs (two SMs) runs a 256 x 256 tile with the 2-SM tensor
@@ -113,10 +117,9 @@ enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2 };
  * memory holds six stages instead of four.  WIDE: each CTA runs a 256 x 256
  * tile alone, as two 128-row accumulators that share every staged block of
  * the weights (three stages of 64 KiB; an expert's last tile of at most 128
- * rows uses one accumulator); staged rows only (not with
- * MK_GATHER_DIRECT).  AUTO: WIDE with staged rows
- * when T*k >= 256*E (two or more 128-row tiles per expert on average),
- * SINGLE otherwise. */
+ * rows uses one accumulator); with any MK_GATHER_* form.  AUTO: WIDE when
+ * T*k >= 256*E (two or more 128-row tiles per expert on average), SINGLE
+ * otherwise. */
 enum { MK_MMA_AUTO = 0, MK_MMA_SINGLE = 1, MK_MMA_PAIR = 2, MK_MMA_WIDE = 3 };
 
 /* Per-launch facts, for tests and the benchmark. */
@@ -127,7 +130,7 @@ typedef struct mk_launch_info {
     int32_t n_group;
     int64_t workspace_bytes;
     int32_t mma_pair;       /* MK_MMA_SINGLE, MK_MMA_PAIR or MK_MMA_WIDE as resolved */
-    int32_t gather;         /* MK_GATHER_STAGED or MK_GATHER_DIRECT as resolved */
+    int32_t gather;         /* MK_GATHER_STAGED, _DIRECT or _GATHER4 as resolved */
     int32_t route_lanes;    /* lanes sharing each token's experts in routing (1, 2, 4, 8) */
     int32_t route_chunks;   /* routing chunks (224 / route_lanes tokens each) */
 } mk_launch_info_t;

@@ -38,6 +38,7 @@ MK_MMA_WIDE = 3
 MK_GATHER_AUTO = 0
 MK_GATHER_STAGED = 1
 MK_GATHER_DIRECT = 2
+MK_GATHER_GATHER4 = 3
 
 # Entry points declared in include/mk.h (checked by the tests).
 ABI_FUNCTIONS = (

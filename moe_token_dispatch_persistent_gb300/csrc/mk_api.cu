@@ -174,7 +174,7 @@ bool wide_shape(int T, int E, int k) { return int64_t(T) * k >= int64_t(2 * BM) 
 // STAGED otherwise (the Mixtral-like layer, k = 2, runs 2% faster staged).
 int resolve_gather(const mk_config_t& c, int T, int H, int E, int k) {
     if (c.mode == MK_MODE_DISPATCH_ONLY) return MK_GATHER_STAGED;
-    if (c.gather != MK_GATHER_AUTO) return c.gather == MK_GATHER_DIRECT ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
+    if (c.gather != MK_GATHER_AUTO) return c.gather;
     if (c.mma_pair == MK_MMA_PAIR || c.mma_pair == MK_MMA_SINGLE) return MK_GATHER_STAGED;
     const bool fits = uint64_t(T) * uint64_t(H) * 2 < (uint64_t(1) << 32);  // 32-bit row offsets into x
     return (k >= 4 && wide_shape(T, E, k) && fits) ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
@@ -301,7 +301,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     for (int i = 0; i < 4; ++i)
         if (c.reserved[i] != 0) return MK_ERR_INVALID_ARG;
     if (c.mma_pair < MK_MMA_AUTO || c.mma_pair > MK_MMA_WIDE) return MK_ERR_INVALID_ARG;
-    if (c.gather < MK_GATHER_AUTO || c.gather > MK_GATHER_DIRECT) return MK_ERR_INVALID_ARG;
+    if (c.gather < MK_GATHER_AUTO || c.gather > MK_GATHER_GATHER4) return MK_ERR_INVALID_ARG;
     if (c.mode < MK_MODE_FUSED || c.mode > MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
     if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
     if (c.debug_fault != MK_FAULT_NONE && c.debug_fault != MK_FAULT_DROP_TILE_FLAG) return MK_ERR_INVALID_ARG;
@@ -327,7 +327,9 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
         return cudaMemsetAsync(expert_offsets, 0, size_t(E + 1) * 4, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
     }
 
-    const bool direct = resolve_gather(c, T, H, E, k) == MK_GATHER_DIRECT;
+    const int gather = resolve_gather(c, T, H, E, k);
+    const bool direct = gather != MK_GATHER_STAGED;  // rows straight from x: cp.async or TMA gather4
+    const bool gather4 = gather == MK_GATHER_GATHER4;
     const int mma = resolve_pair(c, T, E, k);
     const bool pair = mma == MK_MMA_PAIR, wide = mma == MK_MMA_WIDE;
     if (pair && W3) return MK_ERR_UNSUPPORTED;  // the gated FFN runs on single-SM tiles
@@ -380,6 +382,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.mode = c.mode;
     p.compute = c.mode != MK_MODE_DISPATCH_ONLY;
     p.direct = direct ? 1 : 0;
+    p.gather4 = gather4 ? 1 : 0;
     if (c.mode == MK_MODE_DISPATCH_ONLY) {
         p.dispatch_ctas = grid;
     } else if (direct) {
@@ -429,14 +432,16 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
-    // A: the staging rows (staged); encoded over x when there are none (unused then)
+    const uint32_t kbox = BK;  // boxes hold one stage's rows of K
+    // A: the staging rows (staged); with TMA gather4, x itself in boxes one row
+    // high; encoded over x and unused with cp.async rows
     if (encode_2d(&tmA, direct ? x : static_cast<const void*>(p.xs), uint64_t(H), uint64_t(direct ? T : rows),
-                  uint64_t(H) * 2, BK, BM) != CUDA_SUCCESS)
+                  uint64_t(H) * 2, kbox, gather4 ? 1 : BM) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
-    if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+    if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, kbox) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
     CUtensorMap tmB3 = tmB;
-    if (W3 && encode_2d(&tmB3, W3, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+    if (W3 && encode_2d(&tmB3, W3, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, kbox) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
 
     if (p.trace && cudaMemsetAsync(p.trace_buf, 0, size_t(grid) * TRACE_SLOTS * 8, st) != cudaSuccess)
@@ -454,7 +459,7 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     g_last_info.dispatch_ctas = c.mode == MK_MODE_UNFUSED ? 0 : p.dispatch_ctas;
     g_last_info.n_group = p.n_group;
     g_last_info.mma_pair = mma;
-    g_last_info.gather = direct ? MK_GATHER_DIRECT : MK_GATHER_STAGED;
+    g_last_info.gather = gather;
     g_last_info.route_lanes = route_lanes;
     g_last_info.route_chunks = nch;
     g_last_info.workspace_bytes = int64_t(L.total);
@@ -477,13 +482,14 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     for (int i = 0; i < 4; ++i)
         if (c.reserved[i] != 0) return MK_ERR_INVALID_ARG;
     if (c.mma_pair < MK_MMA_AUTO || c.mma_pair > MK_MMA_WIDE) return MK_ERR_INVALID_ARG;
-    if (c.gather < MK_GATHER_AUTO || c.gather > MK_GATHER_DIRECT) return MK_ERR_INVALID_ARG;
+    if (c.gather < MK_GATHER_AUTO || c.gather > MK_GATHER_GATHER4) return MK_ERR_INVALID_ARG;
     if (c.mode < MK_MODE_FUSED || c.mode > MK_MODE_DISPATCH_ONLY) return MK_ERR_INVALID_ARG;
     if (c.out_dtype != MK_OUT_BF16 && c.out_dtype != MK_OUT_F32) return MK_ERR_INVALID_ARG;
     if (c.debug_fault != MK_FAULT_NONE && c.debug_fault != MK_FAULT_DROP_TILE_FLAG) return MK_ERR_INVALID_ARG;
     if (c.dispatch_ctas < 0 || c.grid_ctas < 0 || c.n_group < 0 || c.spin_limit_ns < 0) return MK_ERR_INVALID_ARG;
     // one fused launch, staged rows, tiles on one SM (128-row or wide)
-    if (c.mode != MK_MODE_FUSED || c.gather == MK_GATHER_DIRECT || c.mma_pair == MK_MMA_PAIR)
+    if (c.mode != MK_MODE_FUSED || c.gather == MK_GATHER_DIRECT || c.gather == MK_GATHER_GATHER4 ||
+        c.mma_pair == MK_MMA_PAIR)
         return MK_ERR_UNSUPPORTED;
     const bool wide = resolve_pair(c, T, E, k) == MK_MMA_WIDE;
     if (!expert_offsets || !aligned(expert_offsets, 4)) return MK_ERR_INVALID_ARG;
@@ -593,20 +599,21 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     CUtensorMap tmA[MAX_RANKS], tmB;
     std::memset(tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
+    const uint32_t kbox = BK;  // boxes hold one stage's rows of K
     for (int r = 0; r < ranks; ++r) {
         uint8_t* base = ws + L.rank_base[r];
         p.ep_ctl[r] = reinterpret_cast<EpCtl*>(ws + L.ep_ctl) + r;
         p.ep_counts[r] = reinterpret_cast<int32_t*>(base + L.counts_off);
         p.ep_ready[r] = reinterpret_cast<uint32_t*>(base + L.ready_off);
         p.ep_recv[r] = reinterpret_cast<uint16_t*>(base + L.recv_off);
-        if (encode_2d(&tmA[r], p.ep_recv[r], uint64_t(H), uint64_t(L.cap_rows), uint64_t(H) * 2, BK, BM) !=
+        if (encode_2d(&tmA[r], p.ep_recv[r], uint64_t(H), uint64_t(L.cap_rows), uint64_t(H) * 2, kbox, BM) !=
             CUDA_SUCCESS)
             return MK_ERR_CUDA;
     }
-    if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+    if (encode_2d(&tmB, W, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, kbox) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
     CUtensorMap tmB3 = tmB;
-    if (W3 && encode_2d(&tmB3, W3, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, BK) != CUDA_SUCCESS)
+    if (W3 && encode_2d(&tmB3, W3, uint64_t(F), uint64_t(E) * H, uint64_t(F) * 2, 64, kbox) != CUDA_SUCCESS)
         return MK_ERR_CUDA;
 
     const cudaError_t err = launch_ep(p, tmA, tmB, tmB3, grid, st);

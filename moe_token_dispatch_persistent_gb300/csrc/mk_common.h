@@ -44,12 +44,16 @@ constexpr int PA_STAGE_BYTES = BM * BK * 2;                // 16 KiB (own 128 ro
 constexpr int PB_STAGE_BYTES = BK * (BN / 2) * 2;          // 16 KiB (own 128 columns)
 constexpr int SM_PA = 0;
 constexpr int SM_PB = SM_PA + PSTAGES * PA_STAGE_BYTES;    // 96 KiB
-constexpr int MAX_STAGES = PSTAGES > STAGES ? PSTAGES : STAGES;
 
 // Wide variant (one SM, 256-row tiles, two accumulators sharing each B
 // stage): a stage holds 2 x 16 KiB of A and 32 KiB of B, so three fit.
+// (Six stages of 32 rows of K, the same bytes in finer steps, measured 17%
+// slower on GB300: per row of K the MMA warp waited longer, not shorter.)
 constexpr int WIDE_TILE_M = 2 * BM;
 constexpr int WSTAGES = 3;
+
+constexpr int MAX_STAGES = PSTAGES > STAGES ? (PSTAGES > WSTAGES ? PSTAGES : WSTAGES)
+                                             : (STAGES > WSTAGES ? STAGES : WSTAGES);
 
 // Dynamic shared memory map (offsets from a 1024-byte aligned base).
 constexpr int SM_A = 0;
@@ -167,6 +171,8 @@ struct Params {
     int wide;                // 1: 256-row tiles on one SM, two accumulators sharing each B stage
     int gated;               // 1: y = silu(x.W1) * (x.W3), 128-column N-blocks
     int direct;              // 1: the GEMM's producer copies token rows from x (no staging rows)
+    int gather4;             // with direct: rows arrive by TMA tile::gather4 (tmA maps x, one-row box),
+                             // not by the copy warps' cp.async
     int tile_rows;           // rows per tile: 128, or 256 with pair or wide
     int trace;
     long long spin_limit_ns;

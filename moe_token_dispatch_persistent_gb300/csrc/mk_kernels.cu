@@ -920,7 +920,6 @@ constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN, /*a_mn_major=*/false, /*b_mn_
 // Gated FFN: 128 output columns per item; the item's B stage holds those
 // columns of both projections (gate W1, up W3) side by side.
 constexpr int GATED_BN = BN / 2;
-static_assert(B_STAGE_BYTES / 2 == (GATED_BN / 64) * B_CHUNK_BYTES, "W3 chunks follow the W1 chunks directly");
 
 // One thread's 32 consecutive fp32 results of row `row`, columns [col, col+32),
 // stored as bf16 (round to nearest even) or f32.  Each lane writes its own
@@ -959,6 +958,29 @@ __device__ __forceinline__ void store_row32(const Params& p, size_t row, int col
     }
 }
 
+// Shared-memory stage geometry of the two single-SM tile forms, 64 rows of
+// K per stage.  128-row tiles: four stages of one A block and one B block.
+// Wide (256-row) tiles: three stages of two A blocks and one B block.  A
+// rows are K-major in the 128-byte swizzle (one row = 64 bf16 = one swizzle
+// span); B is N-major, 64-column chunks in the 128-byte swizzle.
+template <bool WIDE>
+struct StageGeo {
+    static constexpr int KB = BK;                      // K per stage
+    static constexpr int NST = WIDE ? WSTAGES : STAGES;
+    static constexpr int ABLK = BM * KB * 2;           // one 128-row A block
+    static constexpr int ASB = (WIDE ? 2 : 1) * ABLK;  // A bytes of a stage
+    static constexpr int BCH = KB * 64 * 2;            // one 64-column B chunk
+    static constexpr int BSB = KB * BN * 2;            // B bytes of a stage
+    static constexpr int SMB = NST * ASB;              // B stages follow the A stages
+    static_assert(SMB + NST * BSB <= SM_STAGE_END, "stages must fit in the stage area");
+    static_assert(NST <= MAX_STAGES, "one full/empty barrier pair per stage");
+    static_assert(BSB / 2 == (GATED_BN / 64) * BCH, "gated: W3 chunks follow the W1 chunks directly");
+};
+
+// Descriptor of a 128-row A block at `addr` (K offset already added):
+// K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t a_desc(uint32_t addr) { return umma_desc_sw128(addr, 16, 1024); }
+
 // Direct-gather producer: COPY_WARPS warps (warp 0, the leader, and warps
 // 6..), no staging rows, no tile flags.  Per item the leader's lane 0 takes a
 // work item from the queue and publishes it; the helpers read it from the
@@ -981,10 +1003,13 @@ template <bool WIDE>
 __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const CUtensorMap* tmB3, CtrlSmem* cs,
                                 const int cw, const WaitCtx& wp) {
     static_assert(!WIDE || COPY_WARPS == 2, "wide tiles: one 128-row block per copy warp");
-    constexpr int NST = WIDE ? WSTAGES : STAGES;
-    constexpr int ASB = WIDE ? 2 * A_STAGE_BYTES : A_STAGE_BYTES;
-    constexpr int SMB = NST * ASB;
+    using G = StageGeo<WIDE>;
+    constexpr int NST = G::NST, ASB = G::ASB, SMB = G::SMB;
     constexpr int ROWS = WIDE ? BM : COPY_ROWS;  // A rows this warp copies per stage
+    constexpr int CPR = G::KB * 2 / 16;          // 16-byte chunks per row and stage: 8
+    constexpr int RPI = 32 / CPR;                // rows per warp instruction: 4
+    static_assert(CPR == 8, "one A row of a stage is one 128-byte swizzle span");
+    const int kblocks = p.H / G::KB;
     const int lane = threadIdx.x & 31;
     const bool leader = cw == 0;
     uint8_t* s = smem_base();
@@ -1033,49 +1058,49 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
         inf.nbk = __shfl_sync(0xffffffffu, inf.nbk, 0);
         // byte offset in x of the tile rows this lane copies (rows past the
         // tile repeat its first row; their products are never stored)
-        uint32_t rowoff[ROWS / 4];
+        uint32_t rowoff[ROWS / RPI];
 #pragma unroll
-        for (int i = 0; i < ROWS / 4; ++i) {
-            const int r = cw * ROWS + 4 * i + (lane >> 3);
+        for (int i = 0; i < ROWS / RPI; ++i) {
+            const int r = cw * ROWS + RPI * i + lane / CPR;
             const int q = __ldcg(p.src_index + inf.row0 + (r < inf.nrows ? r : 0));
             rowoff[i] = uint32_t(min(max(q / p.k, 0), p.T - 1)) * uint32_t(p.H) * 2u;
         }
-        for (int kb = 0; kb < p.kblocks; ++kb) {
+        for (int kb = 0; kb < kblocks; ++kb) {
             if (!warp_wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
                 ok = false;
                 break;
             }
-            if (leader) mbar_arrive_expect_tx_elect(&cs->full[stage], B_STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx_elect(&cs->full[stage], G::BSB);
             __syncwarp();  // the expect-tx before this warp's copies arrive
             uint64_t* fb = &cs->full[stage];
             uint8_t* a = s + stage * ASB + cw * ROWS * 128;
             if (!WIDE || cw * ROWS < inf.nrows) {
-                const int c = lane & 7, rq = lane >> 3;
-                const uint8_t* src = reinterpret_cast<const uint8_t*>(p.x) + kb * (BK * 2) + c * 16;
+                const int c = lane % CPR, rq = lane / CPR;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(p.x) + kb * (G::KB * 2) + c * 16;
+                // 128-byte swizzle: chunk c of row r at r*128 + ((c ^ (r % 8)) * 16)
                 const uint32_t d0 = smem_u32(a) + rq * 128 + ((c ^ rq) << 4);             // rows 4i + rq, i even
                 const uint32_t d1 = smem_u32(a) + (4 + rq) * 128 + ((c ^ (4 + rq)) << 4);  // i odd: row % 8 = 4 + rq
 #pragma unroll
-                for (int i = 0; i < ROWS / 4; ++i)
+                for (int i = 0; i < ROWS / RPI; ++i)
                     cp_async_16_u32(((i & 1) ? d1 - 512 : d0) + 512 * i, src + rowoff[i]);
             }
             cp_async_mbar_arrive_noinc(fb);  // fires once this lane's copies (if any) have landed
             if (leader) {
-                uint8_t* b = s + SMB + stage * B_STAGE_BYTES;
+                uint8_t* b = s + SMB + stage * G::BSB;
                 const int ncol = p.F;
                 if (p.gated) {
 #pragma unroll
                     for (int q = 0; q < GATED_BN / 64; ++q) {
                         const int col = inf.nbk * GATED_BN + q * 64;
                         const int cc = col < ncol ? col : ncol;
-                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, cc, inf.e * p.H + kb * BK, fb);
-                        tma_load_2d_elect(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, cc, inf.e * p.H + kb * BK,
-                                          fb);
+                        tma_load_2d_elect(b + q * G::BCH, tmB, cc, inf.e * p.H + kb * G::KB, fb);
+                        tma_load_2d_elect(b + G::BSB / 2 + q * G::BCH, tmB3, cc, inf.e * p.H + kb * G::KB, fb);
                     }
                 } else {
 #pragma unroll
                     for (int q = 0; q < BN / 64; ++q) {
                         const int col = inf.nbk * BN + q * 64;
-                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * BK,
+                        tma_load_2d_elect(b + q * G::BCH, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * G::KB,
                                           fb);
                     }
                 }
@@ -1093,6 +1118,115 @@ __device__ void producer_direct(const Params& p, const CUtensorMap* tmB, const C
     if (!ok && leader && lane == 0) {
         WaitCtx shortw{nullptr, 0u, 5000000LL};
         for (int st = 0; st < NST; ++st)
+            if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
+    }
+    __syncwarp();
+}
+
+// TMA-gather producer (rows straight from x, one warp): per K-block each
+// lane issues one tile::gather4 per 128-row A block of the stage for rows
+// 4*lane .. 4*lane+3 of that block, so the warp lands the whole block in
+// the A stage's swizzled layout (the tensor map over x has a one-row box of
+// one stage's K, and its swizzle is the A stage's); an elected lane loads
+// the weight chunks as in the staged path.  All of a stage's bytes complete
+// on its full barrier (one arrival: the expect-tx), and the tensor core
+// reads what the async proxy wrote, so no proxy fence is needed.  Rows past
+// the tile's end repeat its first row; their products are never stored.
+template <bool WIDE>
+__device__ void producer_gather4(const Params& p, const CUtensorMap* tmX, const CUtensorMap* tmB,
+                                 const CUtensorMap* tmB3, CtrlSmem* cs, const WaitCtx& wp) {
+    using G = StageGeo<WIDE>;
+    constexpr int NBLK = WIDE ? 2 : 1;  // 128-row A blocks per stage
+    constexpr int RB = G::KB * 2;       // bytes of one A row in a stage
+    static_assert(BM == 4 * 32, "a warp's gather4 loads cover one 128-row block");
+    const int lane = threadIdx.x & 31;
+    uint8_t* s = smem_base();
+    const int total_items = cs->item_start[p.E];
+    const int kblocks = p.H / G::KB;
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_par = 0, issued_any = 0;
+    bool ok = true;
+    uint32_t next = 0;
+    if (lane == 0) next = atom_add_relaxed_u32(&p.ctl->next_item, 1u);
+    next = __shfl_sync(0xffffffffu, next, 0);
+    for (uint32_t it = 0; ok; ++it) {
+        const int item = int(next);
+        const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
+        if (!warp_wait_mbar(&cs->info_empty[slot], iph ^ 1u, wp, SITE_INFO_EMPTY)) {
+            ok = false;
+            break;
+        }
+        if (item >= total_items) {
+            if (lane == 0) {
+                cs->info[slot].e = -1;
+                mbar_arrive(&cs->info_full[slot]);
+            }
+            break;
+        }
+        uint32_t ahead = 0;
+        if (lane == 0) ahead = atom_add_relaxed_u32(&p.ctl->next_item, 1u);  // claimed one item ahead
+        Info inf;
+        int gtile;
+        decode_item(p, cs, item, inf, gtile);
+        if (lane == 0) {
+            cs->info[slot] = inf;
+            mbar_arrive(&cs->info_full[slot]);
+        }
+        const int nblk = (WIDE && inf.nrows > BM) ? 2 : 1;
+        // token of each of this lane's rows: block bl, rows bl*128 + 4*lane + q
+        int tok[NBLK][4];
+#pragma unroll
+        for (int bl = 0; bl < NBLK; ++bl)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = bl * BM + 4 * lane + q;
+                const int sidx = __ldcg(p.src_index + inf.row0 + (r < inf.nrows ? r : 0));
+                tok[bl][q] = min(max(sidx / p.k, 0), p.T - 1);
+            }
+        const int ncol = p.F;
+        for (int kb = 0; kb < kblocks; ++kb) {
+            if (!warp_wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
+                ok = false;
+                break;
+            }
+            uint64_t* fb = &cs->full[stage];
+            mbar_arrive_expect_tx_elect(fb, nblk * G::ABLK + G::BSB);
+            __syncwarp();  // the expect-tx before any of the stage's copies
+            uint8_t* a = s + stage * G::ASB;
+#pragma unroll
+            for (int bl = 0; bl < NBLK; ++bl)
+                if (bl < nblk)
+                    tma_gather4(a + bl * G::ABLK + lane * 4 * RB, tmX, kb * G::KB, tok[bl][0], tok[bl][1], tok[bl][2],
+                                tok[bl][3], fb);
+            uint8_t* b = s + G::SMB + stage * G::BSB;
+            if (p.gated) {
+#pragma unroll
+                for (int q = 0; q < GATED_BN / 64; ++q) {
+                    const int col = inf.nbk * GATED_BN + q * 64;
+                    const int c = col < ncol ? col : ncol;
+                    tma_load_2d_elect(b + q * G::BCH, tmB, c, inf.e * p.H + kb * G::KB, fb);
+                    tma_load_2d_elect(b + G::BSB / 2 + q * G::BCH, tmB3, c, inf.e * p.H + kb * G::KB, fb);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < BN / 64; ++q) {
+                    const int col = inf.nbk * BN + q * 64;
+                    tma_load_2d_elect(b + q * G::BCH, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * G::KB, fb);
+                }
+            }
+            issued_any |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == G::NST) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        next = __shfl_sync(0xffffffffu, ahead, 0);
+    }
+    if (!ok && lane == 0) {
+        // let every issued tensor load land before the CTA can exit
+        WaitCtx shortw{nullptr, 0u, 5000000LL};
+        for (int st = 0; st < G::NST; ++st)
             if (issued_any & (1u << st)) wait_mbar(&cs->full[st], (issued_par >> st) & 1u, shortw, SITE_DRAIN);
     }
     __syncwarp();
@@ -1136,12 +1270,10 @@ template <bool WIDE>
 __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmB3,
                              CtrlSmem* cs, const WorkQueue& wq,
                              bool wait_ready, uint32_t flag, const WaitCtx& w) {
-    constexpr int NST = WIDE ? WSTAGES : STAGES;
-    constexpr int ASB = WIDE ? 2 * A_STAGE_BYTES : A_STAGE_BYTES;  // A bytes of a stage
-    constexpr int SMA = 0, SMB = NST * ASB;
+    using G = StageGeo<WIDE>;
+    constexpr int NST = G::NST, ASB = G::ASB, SMA = 0, SMB = G::SMB;
     constexpr uint32_t NACC = WIDE ? 1u : 2u;  // accumulator buffers
-    static_assert(SMB + NST * B_STAGE_BYTES <= SM_STAGE_END, "stages must fit in the stage area");
-    static_assert(NST <= MAX_STAGES, "one full/empty barrier pair per stage");
+    const int kblocks = p.H / G::KB;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* s = smem_base();
     // Waits inside the pipeline only stall because something upstream (a
@@ -1149,7 +1281,9 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     // that times out and is recorded is the one at the root.
     const WaitCtx wp{w.abort, w.abort_val, w.limit_ns * 2};
 
-    if (p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
+    if (p.direct && p.gather4 && (warp == 0 || warp >= EPI_WARP_END)) {
+        if (warp == 0) producer_gather4<WIDE>(p, tmA, tmB, tmB3, cs, wp);  // the copy helpers idle
+    } else if (p.direct && (warp == 0 || warp >= EPI_WARP_END)) {
         producer_direct<WIDE>(p, tmB, tmB3, cs, warp == 0 ? 0 : warp - EPI_WARP_END + 1, wp);
     } else if (warp == 0) {
         // ---------------- TMA producer: the whole warp runs the loop, one elected lane issues ----------------
@@ -1182,12 +1316,12 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             const int pf = p.l2_prefetch;
             if (pf > 0) {
                 // the first k-blocks of this item's weight slice head for L2 now
-                const int n0 = min(pf, p.kblocks);
+                const int n0 = min(pf, kblocks);
                 for (int kb = 0; kb < n0; ++kb)
 #pragma unroll
                     for (int q = 0; q < BN / 64; ++q) {
                         const int col = inf.nbk * BN + q * 64;
-                        if (col < p.F) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + kb * BK);
+                        if (col < p.F) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + kb * G::KB);
                     }
             }
             if (lane == 0) {
@@ -1212,42 +1346,41 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 fence_proxy_async();
             }
             const int ncol = p.F;
-            for (int kb = 0; kb < p.kblocks; ++kb) {
+            for (int kb = 0; kb < kblocks; ++kb) {
                 if (!warp_wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
                     ok = false;
                     break;
                 }
-                if (pf > 0 && kb + pf < p.kblocks) {
+                if (pf > 0 && kb + pf < kblocks) {
 #pragma unroll
                     for (int q = 0; q < BN / 64; ++q) {
                         const int col = inf.nbk * BN + q * 64;
-                        if (col < ncol) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + (kb + pf) * BK);
+                        if (col < ncol) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + (kb + pf) * G::KB);
                     }
                 }
                 uint64_t* fb = &cs->full[stage];
                 const bool two = WIDE && inf.nrows > BM;  // second 128-row A block
-                mbar_arrive_expect_tx_elect(fb, two ? STAGE_BYTES + A_STAGE_BYTES : STAGE_BYTES);
+                mbar_arrive_expect_tx_elect(fb, (two ? 2 : 1) * G::ABLK + G::BSB);
                 uint8_t* a = s + SMA + stage * ASB;
-                uint8_t* b = s + SMB + stage * B_STAGE_BYTES;
-                tma_load_2d_elect(a, tmA, kb * BK, inf.row0 - wq.a_row0, fb);
-                if (two) tma_load_2d_elect(a + A_STAGE_BYTES, tmA, kb * BK, inf.row0 - wq.a_row0 + BM, fb);
+                uint8_t* b = s + SMB + stage * G::BSB;
+                tma_load_2d_elect(a, tmA, kb * G::KB, inf.row0 - wq.a_row0, fb);
+                if (two) tma_load_2d_elect(a + G::ABLK, tmA, kb * G::KB, inf.row0 - wq.a_row0 + BM, fb);
                 if (p.gated) {
                     // 128 columns of W1 into the first half of the B stage, of W3 into the second
 #pragma unroll
                     for (int q = 0; q < GATED_BN / 64; ++q) {
                         const int col = inf.nbk * GATED_BN + q * 64;
                         const int c = col < ncol ? col : ncol;
-                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, c, inf.e * p.H + kb * BK, fb);
-                        tma_load_2d_elect(b + B_STAGE_BYTES / 2 + q * B_CHUNK_BYTES, tmB3, c, inf.e * p.H + kb * BK,
-                                          fb);
+                        tma_load_2d_elect(b + q * G::BCH, tmB, c, inf.e * p.H + kb * G::KB, fb);
+                        tma_load_2d_elect(b + G::BSB / 2 + q * G::BCH, tmB3, c, inf.e * p.H + kb * G::KB, fb);
                     }
                 } else {
 #pragma unroll
                     for (int q = 0; q < BN / 64; ++q) {
                         const int col = inf.nbk * BN + q * 64;
                         // chunks past F read as zeros (out of bounds fill)
-                        tma_load_2d_elect(b + q * B_CHUNK_BYTES, tmB, col < ncol ? col : ncol,
-                                          inf.e * p.H + kb * BK, fb);
+                        tma_load_2d_elect(b + q * G::BCH, tmB, col < ncol ? col : ncol, inf.e * p.H + kb * G::KB,
+                                          fb);
                     }
                 }
                 issued_any |= 1u << stage;
@@ -1283,31 +1416,31 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             // WIDE: rows 0-127 in TMEM columns [0, 256), rows 128-255 in [256, 512)
             const uint32_t d = cs->tmem_base + acc * BN;
             bool ok = true;
-            for (int kb = 0; kb < p.kblocks; ++kb) {
+            for (int kb = 0; kb < kblocks; ++kb) {
                 if (!warp_wait_mbar(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
                     ok = false;
                     break;
                 }
                 // direct rows were written by cp.async (generic proxy): order
                 // them before the tensor core reads the stage
-                if (p.direct) fence_proxy_async_shared();
+                if (p.direct && !p.gather4) fence_proxy_async_shared();
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(s + SMA + stage * ASB);
-                const uint32_t b0 = smem_u32(s + SMB + stage * B_STAGE_BYTES);
+                const uint32_t b0 = smem_u32(s + SMB + stage * G::BSB);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
+                for (int kk = 0; kk < G::KB / 16; ++kk) {
                     // A: K-major, 128B swizzle, 8-row groups 1024 B apart; +32 B per K=16
-                    const uint64_t ad = umma_desc_sw128(a0 + kk * 32, 16, 1024);
+                    const uint64_t ad = a_desc(a0 + kk * 32);
                     // B: N-major, 128B swizzle; 64-column chunks 8 KiB apart (LBO),
                     // 8-row K groups 1024 B apart (SBO); +2 KiB per K=16
                     // Gated: the stage holds 128 columns of W1 then the same 128
                     // of W3 as four consecutive 64-column chunks, so one N = 256
                     // product leaves A.W1 in accumulator columns [0, 128) and
                     // A.W3 in [128, 256).
-                    const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, B_CHUNK_BYTES, 1024);
+                    const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, G::BCH, 1024);
                     tc_mma_f16_elect(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     if (two)  // the second A block against the same B chunk
-                        tc_mma_f16_elect(d + BN, umma_desc_sw128(a0 + A_STAGE_BYTES + kk * 32, 16, 1024), bd, IDESC,
+                        tc_mma_f16_elect(d + BN, a_desc(a0 + G::ABLK + kk * 32), bd, IDESC,
                                          (kb | kk) != 0 ? 1u : 0u);
                 }
                 issued = true;
@@ -1779,18 +1912,19 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
 }
 
 // Barrier arrival counts.  Single CTA: the producer's expect-tx, one commit,
-// 128 epilogue threads, the MMA thread + 4 epilogue warps.  Direct gather
-// adds one cp.async arrival per copy lane to each full barrier and one
-// info_empty arrival per copy helper warp.  Pair: acc_empty
+// 128 epilogue threads, the MMA thread + 4 epilogue warps.  Direct rows by
+// cp.async (copy_warps) add one cp.async arrival per copy lane to each full
+// barrier and one info_empty arrival per copy helper warp; rows by TMA
+// gather4 add none.  Pair: acc_empty
 // gets one arrival per epilogue warp of both CTAs (8) and info_empty the
 // leader's MMA thread and 4 epilogue warps plus the peer's producer and 4
 // epilogue warps (10); those two live in the leader only.
 template <int PAIR>
-__device__ void cta_setup(CtrlSmem* cs, bool with_tmem, bool direct) {
+__device__ void cta_setup(CtrlSmem* cs, bool with_tmem, bool copy_warps) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int i = 0; i < MAX_STAGES; ++i) {
-            mbar_init(&cs->full[i], direct ? 1 + 32 * COPY_WARPS : 1);
+            mbar_init(&cs->full[i], copy_warps ? 1 + 32 * COPY_WARPS : 1);
             mbar_init(&cs->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1799,7 +1933,7 @@ __device__ void cta_setup(CtrlSmem* cs, bool with_tmem, bool direct) {
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&cs->info_full[i], 1);
-            mbar_init(&cs->info_empty[i], PAIR ? 10 : 1 + 4 + (direct ? COPY_WARPS - 1 : 0));
+            mbar_init(&cs->info_empty[i], PAIR ? 10 : 1 + 4 + (copy_warps ? COPY_WARPS - 1 : 0));
         }
         mbar_init(&cs->drain, 1);
         for (int i = 0; i < MAX_GATHER_SLOTS; ++i) mbar_init(&cs->gbar[i], 1);
@@ -1908,7 +2042,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (PAIR && !in_cta_pair(p, w)) return;
-    cta_setup<PAIR>(cs, p.compute != 0, p.direct != 0);
+    cta_setup<PAIR>(cs, p.compute != 0, p.direct != 0 && p.gather4 == 0);
 
     // This call's readiness flags start at 0.  Cleared before the routing
     // barrier; they are set only after it, so no stale value is ever seen.
@@ -2177,7 +2311,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (PAIR && !in_cta_pair(p, w)) return;
-    cta_setup<PAIR>(cs, true, p.direct != 0);
+    cta_setup<PAIR>(cs, true, p.direct != 0 && p.gather4 == 0);
     for (int e = threadIdx.x; e < p.E; e += NTHREADS) cs->tot[e] = p.expert_offsets[e + 1] - p.expert_offsets[e];
     __syncthreads();
     build_tables(p, cs);

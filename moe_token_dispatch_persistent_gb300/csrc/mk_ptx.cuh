@@ -136,6 +136,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// TMA tile::gather4: rows r0..r3 of a 2-D tensor (the map's box is one row
+// high), columns [c0, c0 + box width), land as four consecutive box rows at
+// smem_dst in the map's swizzle, completing their bytes on `bar`.  Issued by
+// the calling thread (any number of lanes may each issue their own).
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* m, int32_t c0, int32_t r0, int32_t r1,
+                                            int32_t r2, int32_t r3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Prefetch a 2-D tensor box into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t c0, int32_t c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -73,6 +73,9 @@ def parse_args(argv=None):
     ap.add_argument("--experts-div", type=int, default=1,
                     help="small case for profiler captures: E/D experts and T/D tokens, H, F, k and the value "
                          "recipe unchanged (not a bench workload)")
+    ap.add_argument("--h-div", type=int, default=1,
+                    help="small case for profiler captures: H/D, everything else unchanged, so routing and the "
+                         "rows of every expert stay those of the full layer (not a bench workload)")
     return ap.parse_args(argv)
 
 
@@ -139,6 +142,19 @@ def reduced_workload(w: synth.Workload, d: int) -> synth.Workload:
     if d < 1 or w.E % d or w.T % d or w.E // d < 32:
         raise SystemExit(f"--experts-div {d}: needs a divisor of E={w.E} and T={w.T} leaving at least 32 experts")
     return synth.Workload(f"{w.name}_experts_div_{d}", w.T // d, w.H, w.F, w.E // d, w.k, w.seed, w.kind)
+
+
+def reduced_hidden(w: synth.Workload, d: int) -> synth.Workload:
+    """The same layer with H/d: T, E, k, F, the seed and the logits recipe
+    stay, so routing, the active experts and every expert's rows are those
+    of the full layer while the weights shrink d-fold.  A small case of the
+    same kernel for profiler captures of a skewed or decode layer whose full
+    weights hold many GB on the device."""
+    if d == 1:
+        return w
+    if d < 1 or w.H % (64 * d):
+        raise SystemExit(f"--h-div {d}: H={w.H} / {d} must stay a multiple of 64")
+    return synth.Workload(f"{w.name}_h_div_{d}", w.T, w.H // d, w.F, w.E, w.k, w.seed, w.kind)
 
 
 def compulsory_bytes(w: synth.Workload, active_experts: int) -> int:
@@ -792,7 +808,7 @@ def run_ours(args, w):
         # every workload, one at a time (one GPU only: under torchrun each rank
         # would repeat the whole set)
         wanted = [] if args.configs.strip().lower() == "none" else [int(c) for c in args.configs.split(",") if c]
-        if world == 1 and args.experts_div == 1 and wanted:
+        if world == 1 and args.experts_div == 1 and args.h_div == 1 and wanted:
             per = {}
             for cid in wanted:
                 wc = synth.WORKLOADS[cid]
@@ -818,7 +834,7 @@ def run_ours(args, w):
 
 def main(argv=None):
     args = parse_args(argv)
-    w = reduced_workload(synth.WORKLOADS[args.config], args.experts_div)
+    w = reduced_hidden(reduced_workload(synth.WORKLOADS[args.config], args.experts_div), args.h_div)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -74,8 +74,9 @@ enum {
 
 enum { MK_OUT_BF16 = 0, MK_OUT_F32 = 1 };
 
-/* Host-side fault injection (never a device trap): withhold the readiness
- * flag of one tile so the compute role's bounded wait runs out. */
+/* Host-side fault injection (never a device trap): withhold the arrival of
+ * one tile's rows (its readiness never completes) so the compute role's
+ * bounded wait runs out. */
 enum { MK_FAULT_NONE = 0, MK_FAULT_DROP_TILE_FLAG = 1 };
 
 typedef struct mk_config {
@@ -97,8 +98,9 @@ typedef struct mk_config {
 } mk_config_t;
 
 /* Token rows for the GEMM.  STAGED: dispatch CTAs copy them into
- * expert-contiguous tiles in the workspace and release a flag per tile;
- * compute CTAs wait on the flag and load whole tiles.  DIRECT: the GEMM's
+ * expert-contiguous tiles in the workspace, in units of up to 32 rows, and
+ * add each unit's rows to its tile's arrival count; compute CTAs wait until
+ * a tile's count reaches its rows and load whole tiles.  DIRECT: the GEMM's
  * producer warp copies each tile's rows straight from x into its
  * shared-memory stages (16-byte cp.async), so there is no staging copy, no
  * gather role, and the workspace holds no staging rows (T*k*H*2 bytes

@@ -59,9 +59,16 @@ constexpr int MAX_STAGES = PSTAGES > STAGES ? (PSTAGES > WSTAGES ? PSTAGES : WST
 constexpr int SM_A = 0;
 constexpr int SM_B = SM_A + STAGES * A_STAGE_BYTES;           // 64 KiB
 constexpr int SM_STAGE_END = SM_B + STAGES * B_STAGE_BYTES;   // 192 KiB
-constexpr int SM_CTRL = SM_STAGE_END;
+// Epilogue output buffers: one 32-row x 64-column bf16 box (4 KiB, 128-byte
+// swizzle) per epilogue warp, the source of its tensor stores.
+constexpr int EPI_BOX_COLS = 64;
+constexpr int EPI_BOX_ROWS = 32;
+constexpr int EPI_BUF_BYTES = EPI_BOX_COLS * EPI_BOX_ROWS * 2;
+constexpr int SM_EPI = SM_STAGE_END;
+constexpr int SM_CTRL = SM_EPI + 4 * EPI_BUF_BYTES;           // 208 KiB
 constexpr int SM_CTRL_BYTES = 8192;
 constexpr int SMEM_BYTES = SM_CTRL + SM_CTRL_BYTES + 1024;    // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "dynamic shared memory of one CTA on sm_103");
 
 // Routing scratch aliases the stage area (routing ends before the GEMM).
 constexpr int RT_LOGIT_STRIDE = 65;                           // 64 experts per pass + 1 pad
@@ -81,7 +88,7 @@ static_assert(SM_PB + PSTAGES * PB_STAGE_BYTES <= SM_STAGE_END, "pair stages mus
 
 // Control block at the head of the workspace.  The kernels leave it ready
 // for the next call: the last CTA to exit zeroes the counters and the abort
-// word.  Readiness flags are cleared by the fused kernel itself.
+// word.  Tile arrival counts are cleared by the fused kernel itself.
 struct Ctl {
     uint32_t epoch;
     uint32_t exit_count;
@@ -92,7 +99,8 @@ struct Ctl {
     uint32_t abort;          // 1 once any CTA of this call gave up
     uint32_t tiles_done;     // tiles the dispatch role has gathered and flagged
     uint32_t bar_computed;   // CTAs done with the GEMM (combine barrier)
-    uint32_t pad[55];
+    uint32_t bar_scanned;    // CTAs whose expert columns are scanned (distributed scan)
+    uint32_t pad[54];
 };
 static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");
 
@@ -136,6 +144,7 @@ enum Site : int {
     SITE_EP_RETURNED = 17,
     SITE_PAIR_ALIGN = 18,
     SITE_PAIR_CLUSTER = 19,
+    SITE_BAR_SCANNED = 20,
 };
 
 enum ErrCode : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_FAULT = 2 };
@@ -153,6 +162,7 @@ struct Params {
     int T, H, F, E, k;
     int out_f32;
     int y_v8;                // y is 32-byte aligned: results go out as 256-bit stores
+    int y_tma;               // whole 32-row groups go out as tensor stores (tmY: bf16 y_sorted)
     // derived sizes
     int rows;                // T*k
     int nch;                 // routing chunks
@@ -174,6 +184,8 @@ struct Params {
     int gather4;             // with direct: rows arrive by TMA tile::gather4 (tmA maps x, one-row box),
                              // not by the copy warps' cp.async
     int tile_rows;           // rows per tile: 128, or 256 with pair or wide
+    int dist_scan;           // 1: each CTA scans whole expert columns of the count table
+                             // (bases, totals), a barrier, then every CTA reads the totals
     int trace;
     long long spin_limit_ns;
     // workspace
@@ -182,10 +194,12 @@ struct Params {
     int32_t* topk_idx;       // [T*k]
     float* topk_gate;        // [T*k]
     int32_t* lrank;          // [T*k]
-    int32_t* bases;          // [nch][E] (unfused path)
+    int32_t* bases;          // [nch][E] rows of earlier chunks per expert (unfused path,
+                             // distributed scan)
+    int32_t* totals;         // [E] rows per expert (distributed scan)
     int32_t* row_of;         // [T*k] sorted row of each (t, j)
     void* combine_out;       // [T,F] (y_sorted's dtype) or null: no combine
-    uint32_t* ready;         // [max_tiles]
+    uint32_t* ready;         // [max_tiles] rows of each tile gathered so far (staged rows)
     uint16_t* xs;            // [T*k,H] bf16 staging
     unsigned long long* trace_buf;  // [grid][TRACE_SLOTS]
     int max_tiles;
@@ -219,7 +233,7 @@ struct Params {
 
 // Workspace carve-up, shared by the size query and the launcher.
 struct WsLayout {
-    size_t ctl, counts, topk_idx, topk_gate, lrank, row_of, bases, ready, trace, xs, total;
+    size_t ctl, counts, topk_idx, topk_gate, lrank, row_of, bases, totals, ready, trace, xs, total;
 };
 
 inline size_t ws_align(size_t v) { return (v + 255) & ~size_t(255); }
@@ -230,20 +244,23 @@ constexpr int MAX_GRID = 1024;
 // experts are split over S lanes (S * 32 or S * 64 experts, read with
 // 16-byte loads), so a chunk holds ROUTE_CHUNK / S tokens and S times as
 // many CTAs route.  S is the largest split whose chunks still number at
-// most one per CTA and whose count table (chunks x E) stays within 20480
-// counts: every CTA scans the whole table, and on GB300 a 147 x 256 table
-// cost more scan time than the split saved in routing.  S = 1 (a lane per
-// token) for other expert counts, for logits that are not 16-byte aligned,
-// or when no split passes both limits.
+// most one per CTA (routing time is per chunk).  S = 1 (a lane per token)
+// for other expert counts, for logits that are not 16-byte aligned, or
+// when no split passes.  Large count tables (chunks x E) are scanned by
+// columns across the CTAs (DIST_SCAN_COUNTS), so the table size sets no
+// limit here.
 inline int route_lanes_for(int T, int E, int grid, bool logits_16b) {
     if (!logits_16b) return 1;
     int S = E == 64 ? 2 : E == 128 ? 4 : E == 256 ? MAX_ROUTE_LANES : 1;
     while (S > 1 && (int64_t(T) + ROUTE_CHUNK / S - 1) / (ROUTE_CHUNK / S) > grid) S >>= 1;
-    // the scan reads every chunk's counts: at most 20480 of them (80 KiB)
-    while (S > 1 && (int64_t(T) + ROUTE_CHUNK / S - 1) / (ROUTE_CHUNK / S) * E > 20480) S >>= 1;
     if (S > 1 && E / S > 64) S = 1;  // a lane scans 32 or 64 experts
     return S;
 }
+
+// Count tables of more than this many entries are scanned by columns, each
+// CTA one expert at a time (a second grid barrier, but no CTA reads the
+// whole table); smaller ones by every CTA from a copy in shared memory.
+constexpr int DIST_SCAN_COUNTS = 4096;
 
 // Routing chunks of a call: with S > 1 there are at most `grid` of them.
 inline size_t route_chunks_bound(int T) {
@@ -266,6 +283,7 @@ inline WsLayout ws_layout(int T, int H, int E, int k, bool staging = true, int g
     L.lrank = o;      o = ws_align(o + rows * 4);
     L.row_of = o;     o = ws_align(o + rows * 4);
     L.bases = o;      o = ws_align(o + nch * E * 4);
+    L.totals = o;     o = ws_align(o + size_t(E) * 4);
     L.ready = o;      o = ws_align(o + max_tiles * 4);
     L.trace = o;      o = ws_align(o + size_t(grid) * TRACE_SLOTS * 8);
     L.xs = o;         o = ws_align(o + (staging ? rows * size_t(H) * 2 : 0));

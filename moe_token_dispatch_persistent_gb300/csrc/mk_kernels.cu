@@ -17,10 +17,11 @@
 //   phase S  (all CTAs)    per-expert totals, exclusive scan -> offsets,
 //                           tile and work-item tables (each CTA, in smem);
 //                           scatter src_index / gate_w of the CTA's chunks
-//   dispatch role          pull-gather: tiles taken in GEMM consumption
-//                           order, rows moved with 1-D bulk copies through
-//                           shared memory, a release flag per finished tile;
-//                           then the CTA joins the compute role
+//   dispatch role          pull-gather: units of up to 32 rows of a tile
+//                           taken in GEMM consumption order, rows moved with
+//                           1-D bulk copies through shared memory, each
+//                           unit's row count added to its tile's arrival
+//                           count (release); then the CTA joins compute
 //   compute role           TMA producer warp -> mbarrier ring -> MMA warp
 //                           (tcgen05.mma 128x256x16, fp32 in TMEM; both
 //                           loops run on whole warps, one elected lane
@@ -661,6 +662,64 @@ __device__ void scan_counts(const Params& p, CtrlSmem* cs, const int32_t* counts
     __syncthreads();
 }
 
+// Distributed scan, step 1 (CTA b): for the experts e = b, b + grid, ... the
+// exclusive prefix over chunks of count[c][e] goes to bases[c][e] and the
+// column total to totals[e].  Thread i holds the consecutive chunks
+// [i*per, (i+1)*per): a pass over them for its sum, a block-wide exclusive
+// scan of the sums (warp shuffles, then the warps' totals), a second pass
+// writing the prefixes.
+__device__ void scan_columns(const Params& p) {
+    int* wsum = reinterpret_cast<int*>(smem_base());  // per-warp sums (routing scratch is dead)
+    const int nch = p.nch, E = p.E;
+    const int per = (nch + NTHREADS - 1) / NTHREADS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = threadIdx.x * per;
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        int sum = 0;
+        for (int i = 0; i < per; ++i) {
+            const int c = c0 + i;
+            if (c < nch) sum += __ldcg(p.counts + size_t(c) * E + e);
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int run = incl - sum;
+        for (int w = 0; w < warp; ++w) run += wsum[w];
+        for (int i = 0; i < per; ++i) {
+            const int c = c0 + i;
+            if (c < nch) {
+                p.bases[size_t(c) * E + e] = run;
+                run += __ldcg(p.counts + size_t(c) * E + e);
+            }
+        }
+        if (threadIdx.x == NTHREADS - 1) p.totals[e] = run;  // the last thread's run covers every chunk
+        __syncthreads();
+    }
+}
+
+// Distributed scan, step 2 (after the barrier): the totals give every CTA
+// its offset, tile and item tables; the bases of its own chunks (c_first,
+// c_first + c_stride, ... below c_end) are offs[e] + bases[c][e], kept in
+// shared memory as scan_counts keeps them.
+__device__ void scan_from_columns(const Params& p, CtrlSmem* cs, int c_first, int c_stride, int c_end) {
+    int* sbase = reinterpret_cast<int*>(smem_base() + RT_BASES);
+    const int E = p.E;
+    for (int e = threadIdx.x; e < E; e += NTHREADS) cs->tot[e] = __ldcg(p.totals + e);
+    __syncthreads();
+    build_tables(p, cs);
+    __syncthreads();
+    int m = 0;
+    for (int c = c_first; c < c_end; c += c_stride, ++m)
+        for (int e = threadIdx.x; e < E; e += NTHREADS)
+            sbase[m * MAX_E + e] = cs->offs[e] + __ldcg(p.bases + size_t(c) * E + e);
+    __syncthreads();
+}
+
 // Scatter src_index / gate_w for (t, j) entries of chunk c (bases in smem).
 __device__ void scatter_chunk(const Params& p, int c, const int* cbase, const WaitCtx& w) {
     const int k = p.k;
@@ -710,65 +769,95 @@ __device__ __forceinline__ int find_expert(const int32_t* starts, int E, int v) 
     return lo;
 }
 
-// Dispatch role: pull tiles (GEMM consumption order) from the gather queue;
-// each of `gather_slots` lanes of warp 0 moves one row at a time
-// x[src] -> smem -> xs[row] with bulk copies; the tile's flag is released
-// once all its rows are written.
-__device__ void gather_role(const Params& p, CtrlSmem* cs, uint32_t flag, const WaitCtx& w) {
+// Dispatch role (warp 0): pull gather units from the queue in GEMM
+// consumption order.  A unit is up to `gather_slots` rows of one tile, one
+// row per slot lane, so several dispatch CTAs fill a tile at once and its
+// first items start soon after the scan.  Each lane moves its row
+// x[src] -> smem -> xs[row] with bulk copies and closes one bulk group per
+// unit (empty when it had no row).  A CTA's first unit is published as soon
+// as its stores complete (the first tiles gate the GEMM's start); after
+// that a unit's stores are waited for one unit later, while the next unit's
+// loads are in flight.  Publishing adds the unit's rows to the tile's
+// arrival count (release); the unit that completes a tile also counts it in
+// tiles_done.
+__device__ __forceinline__ void publish_unit(const Params& p, int tile, int n, int trows) {
+    if (tile == p.debug_drop_tile) return;  // host-side fault injection: this tile never completes
+    __threadfence();
+    const uint32_t before = atom_add_acq_rel_u32(p.ready + tile, uint32_t(n));
+    // once tiles_done reaches the tile count, one acquire of it stands in for
+    // every tile's arrival count
+    if (before + uint32_t(n) == uint32_t(trows)) atom_add_acq_rel_u32(&p.ctl->tiles_done, 1u);
+}
+
+__device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp != 0) return;
     uint8_t* s = smem_base();
     const uint32_t row_bytes = uint32_t(p.H) * 2u;
-    const int nslot = p.gather_slots;
-    const int ntiles = cs->tile_start[p.E];
+    const int unit = p.gather_slots;                  // rows per unit: one per slot lane
+    const int upt = (p.tile_rows + unit - 1) / unit;  // units per tile
+    const int nunits = cs->tile_start[p.E] * upt;
+    uint8_t* slot = s + size_t(lane) * row_bytes;
     uint32_t ph = 0;
-    bool ok = true;
-    while (ok) {
-        int tile = 0;
-        if (lane == 0) tile = int(atom_add_relaxed_u32(&p.ctl->next_tile, 1u));
-        tile = __shfl_sync(0xffffffffu, tile, 0);
-        if (tile >= ntiles) break;
-        const int e = find_expert(cs->tile_start, p.E, tile);
-        const int row0 = cs->offs[e] + (tile - cs->tile_start[e]) * p.tile_rows;
-        const int nrows = min(p.tile_rows, cs->offs[e + 1] - row0);
-        if (lane < nslot) {
-            uint8_t* slot = s + size_t(lane) * row_bytes;
-            for (int i = lane; i < nrows && ok; i += nslot) {
-                const int r = row0 + i;
+    bool ok = true, first = true;
+    int pend_tile = -1, pend_n = 0, pend_rows = 0;    // the unit whose stores may still be in flight
+    for (;;) {
+        int u = 0;
+        if (lane == 0) u = int(atom_add_relaxed_u32(&p.ctl->next_tile, 1u));
+        u = __shfl_sync(0xffffffffu, u, 0);
+        const bool have = ok && u < nunits && !aborted(w);
+        int tile = -1, n = 0, trows = 0;
+        if (have) {
+            tile = u / upt;
+            const int e = find_expert(cs->tile_start, p.E, tile);
+            const int row0 = cs->offs[e] + (tile - cs->tile_start[e]) * p.tile_rows;
+            trows = min(p.tile_rows, cs->offs[e + 1] - row0);
+            const int r0 = (u - tile * upt) * unit;
+            n = max(0, min(unit, trows - r0));
+            if (lane < n) {
+                const int r = row0 + r0 + lane;
                 const int src_t = __ldcg(p.src_index + r) / p.k;
                 if (src_t < 0 || src_t >= p.T) {
                     record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(r));
                     raise_abort(w);
                     ok = false;
-                    break;
-                }
-                bulk_wait_read<0>();
-                mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
-                bulk_load(slot, p.x + size_t(src_t) * p.H, row_bytes, &cs->gbar[lane]);
-                if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
-                    ok = false;
-                    // the load is in flight: give it a short, bounded chance to land
-                    WaitCtx shortw{nullptr, 0u, 2000000LL};
-                    wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
-                }
-                ph ^= 1u;
-                if (ok) {
-                    bulk_store(p.xs + size_t(r) * p.H, slot, row_bytes);
-                    bulk_commit();
+                } else {
+                    bulk_wait_read<0>();  // the slot's previous store has read it
+                    mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
+                    bulk_load(slot, p.x + size_t(src_t) * p.H, row_bytes, &cs->gbar[lane]);
+                    if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
+                        ok = false;
+                        // the load is in flight: give it a short, bounded chance to land
+                        WaitCtx shortw{nullptr, 0u, 2000000LL};
+                        wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
+                    }
+                    ph ^= 1u;
+                    if (ok) bulk_store(p.xs + size_t(r) * p.H, slot, row_bytes);
                 }
             }
-            bulk_wait_all();
-            fence_proxy_async();
         }
+        bulk_commit();  // this unit's group (empty without a row)
         ok = __all_sync(0xffffffffu, ok);
-        if (lane == 0 && ok && tile != p.debug_drop_tile) {
-            __threadfence();
-            st_release_u32(p.ready + tile, flag);
-            // count of tiles gathered so far: once it reaches the tile count a
-            // single acquire of it stands in for every per-tile flag
-            atom_add_acq_rel_u32(&p.ctl->tiles_done, 1u);
+        if (first && have && n > 0) {
+            // the CTA's first unit: publish it without waiting for the next
+            bulk_wait<0>();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0 && ok) publish_unit(p, tile, n, trows);
+            first = false;
+            continue;
         }
-        if (aborted(w)) break;
+        if (pend_tile >= 0) {
+            // the previous unit's group is complete once at most this one is pending
+            bulk_wait<1>();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0 && ok) publish_unit(p, pend_tile, pend_n, pend_rows);
+        }
+        pend_tile = (have && n > 0) ? tile : -1;
+        pend_n = n;
+        pend_rows = trows;
+        if (!have) break;
     }
     bulk_wait_all();
 }
@@ -980,6 +1069,71 @@ struct StageGeo {
 // Descriptor of a 128-row A block at `addr` (K offset already added):
 // K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t a_desc(uint32_t addr) { return umma_desc_sw128(addr, 16, 1024); }
+
+// Epilogue of 32 whole rows (TMEM lanes of this warp, all inside the tile)
+// through shared memory and tensor stores.  Per 64-column chunk the warp
+// reads its accumulator columns (for the gated FFN: the W1 and W3 halves,
+// SwiGLU applied), rounds them to bf16 and writes its 32 rows into its own
+// 4 KiB buffer in the 128-byte swizzle (lane = row, chunk c of row r at
+// r*128 + ((c ^ (r % 8)) * 16): conflict-free), and one lane stores the
+// 32 x 64 box with one TMA store.  A buffer is rewritten only after the
+// previous store has read it.  Each row's 32 stores of 32 bytes per item
+// (one per lane and instruction, 32 rows apart) become whole 128-byte lines.
+__device__ __forceinline__ void epi_rows_tma(const Params& p, const CUtensorMap* tmY, uint8_t* buf, uint32_t tbase,
+                                             int n0, int row_first) {
+    const int lane = threadIdx.x & 31;
+    const int nchunks = (p.gated ? GATED_BN : BN) / EPI_BOX_COLS;
+#pragma unroll 1
+    for (int c64 = 0; c64 < nchunks; ++c64) {
+        const int col = n0 + c64 * EPI_BOX_COLS;
+        if (col >= p.F) break;
+        uint32_t pk[32];
+        if (p.gated) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32], r3[32];
+                tmem_ld_32x32b_x32(tbase + c64 * 64 + h * 32, r);
+                tmem_ld_32x32b_x32(tbase + GATED_BN + c64 * 64 + h * 32, r3);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    // SwiGLU as in the per-row epilogue: silu(a) * b, fast intrinsics
+                    const float a0 = __uint_as_float(r[2 * u]), a1 = __uint_as_float(r[2 * u + 1]);
+                    const float v0 = __fdividef(a0, 1.f + __expf(-a0)) * __uint_as_float(r3[2 * u]);
+                    const float v1 = __fdividef(a1, 1.f + __expf(-a1)) * __uint_as_float(r3[2 * u + 1]);
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+                    pk[16 * h + u] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+            }
+        } else {
+            uint32_t r[32], r2[32];
+            tmem_ld_32x32b_x32(tbase + c64 * 64, r);
+            tmem_ld_32x32b_x32(tbase + c64 * 64 + 32, r2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+                const __nv_bfloat162 b1 =
+                    __floats2bfloat162_rn(__uint_as_float(r2[2 * u]), __uint_as_float(r2[2 * u + 1]));
+                pk[u] = *reinterpret_cast<const uint32_t*>(&b0);
+                pk[16 + u] = *reinterpret_cast<const uint32_t*>(&b1);
+            }
+        }
+        if (lane == 0) bulk_wait_read<0>();  // the previous box has left the buffer
+        __syncwarp();
+        const uint32_t rowaddr = smem_u32(buf) + uint32_t(lane) * 128u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4(rowaddr + ((uint32_t(c) ^ uint32_t(lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                         pk[4 * c + 3]);
+        fence_proxy_async_shared();  // the generic writes before the tensor store reads them
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmY, buf, col, row_first);
+            bulk_commit();
+        }
+    }
+}
 
 // Direct-gather producer: COPY_WARPS warps (warp 0, the leader, and warps
 // 6..), no staging rows, no tile flags.  Per item the leader's lane 0 takes a
@@ -1268,7 +1422,7 @@ __device__ __forceinline__ int rank_of_token(const Params& p, int t) {
 // and loads one A block.
 template <bool WIDE>
 __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmB3,
-                             CtrlSmem* cs, const WorkQueue& wq,
+                             const CUtensorMap* tmY, CtrlSmem* cs, const WorkQueue& wq,
                              bool wait_ready, uint32_t flag, const WaitCtx& w) {
     using G = StageGeo<WIDE>;
     constexpr int NST = G::NST, ASB = G::ASB, SMA = 0, SMB = G::SMB;
@@ -1336,10 +1490,11 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 }
                 fence_proxy_async();
             } else if (wait_ready) {
-                // one acquire per item until every tile is known to be in
+                // one acquire per item until every tile is known to be in;
+                // before that, the tile's arrival count reaches its rows
                 if (__all_sync(0xffffffffu, ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles))) {
                     wait_ready = false;
-                } else if (!warp_wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
+                } else if (!warp_wait_geq(p.ready + gtile, uint32_t(inf.nrows), w, SITE_TILE_READY)) {
                     ok = false;
                     break;
                 }
@@ -1487,7 +1642,11 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 const int ep_q = (p.ep && rowok) ? __ldcg(p.src_index + inf.row0 + rloc) : -1;
                 const size_t row = p.ep ? size_t(ep_q < 0 ? 0 : ep_q) : size_t(inf.row0) + rloc;
                 const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + (acc + half) * BN;
-                if (p.gated) {
+                if (tmY != nullptr && p.y_tma && half * BM + quad * 32 + 32 <= inf.nrows) {
+                    // all 32 rows of this warp lie in the tile: tensor stores
+                    epi_rows_tma(p, tmY, s + SM_EPI + (warp - 2) * EPI_BUF_BYTES, tbase,
+                                 inf.nbk * (p.gated ? GATED_BN : BN), inf.row0 + half * BM + quad * 32);
+                } else if (p.gated) {
                     const int n0 = inf.nbk * GATED_BN;
 #pragma unroll 1
                     for (int cc = 0; cc < GATED_BN / 32; ++cc) {
@@ -1554,6 +1713,13 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 accph ^= 1u;
             }
         }
+        if (lane == 0) {
+            // this warp's tensor stores have landed (visible to the combine
+            // and to later kernels) before the role ends
+            bulk_wait_all();
+            fence_proxy_async();
+        }
+        __syncwarp();
     }
 }
 
@@ -1786,7 +1952,7 @@ __device__ void compute_role_pair(const Params& p, const CUtensorMap* tmA, const
             if (wait_ready) {
                 if (__all_sync(0xffffffffu, ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles))) {
                     wait_ready = false;
-                } else if (!warp_wait_eq(p.ready + gtile, flag, w, SITE_TILE_READY)) {
+                } else if (!warp_wait_geq(p.ready + gtile, uint32_t(inf.nrows), w, SITE_TILE_READY)) {
                     ok = false;
                     break;
                 }
@@ -1985,6 +2151,7 @@ __device__ void cta_exit(const Params& p) {
             c->next_item = 0;
             c->tiles_done = 0;
             c->bar_computed = 0;
+            c->bar_scanned = 0;
             c->abort = 0;
             c->epoch = c->epoch + 1u;  // calls completed on this workspace
             if (p.stream_flag) {
@@ -2031,7 +2198,7 @@ __device__ bool in_cta_pair(const Params& p, const WaitCtx& w) {
 template <int PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mk_fused_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB3) {
+                    const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmY) {
     CtrlSmem* cs = ctrl();
     const uint32_t flag = 1u;  // tile ready / call aborted
     const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
@@ -2044,8 +2211,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (PAIR && !in_cta_pair(p, w)) return;
     cta_setup<PAIR>(cs, p.compute != 0, p.direct != 0 && p.gather4 == 0);
 
-    // This call's readiness flags start at 0.  Cleared before the routing
-    // barrier; they are set only after it, so no stale value is ever seen.
+    // This call's tile arrival counts start at 0.  Cleared before the routing
+    // barrier; they grow only after it, so no stale value is ever seen.
     for (int i = blockIdx.x * NTHREADS + threadIdx.x; i < p.max_tiles; i += gridDim.x * NTHREADS) p.ready[i] = 0u;
     if (p.stream_done) {
         const int nchunks = (p.rows + p.stream_rows - 1) / p.stream_rows;
@@ -2066,9 +2233,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ok = cs->bcast[0] != 0;
     stamp(p, 2);
 
+    if (ok && p.dist_scan) {
+        // phase S on a large count table: columns across the CTAs, then a barrier
+        scan_columns(p);
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atom_add_acq_rel_u32(&p.ctl->bar_scanned, 1u);
+            ok = wait_geq(&p.ctl->bar_scanned, gridDim.x, w, SITE_BAR_SCANNED);
+            cs->bcast[0] = ok;
+        }
+        __syncthreads();
+        ok = cs->bcast[0] != 0;
+    }
     if (ok) {
         // phase S
-        scan_counts(p, cs, p.counts, true, blockIdx.x, gridDim.x, p.nch, -1);
+        if (p.dist_scan) scan_from_columns(p, cs, blockIdx.x, gridDim.x, p.nch);
+        else scan_counts(p, cs, p.counts, true, blockIdx.x, gridDim.x, p.nch, -1);
         if (blockIdx.x == 0)
             for (int e = threadIdx.x; e <= p.E; e += NTHREADS) p.expert_offsets[e] = cs->offs[e];
         if (threadIdx.x == 0 && cs->offs[p.E] != p.rows) {
@@ -2090,7 +2270,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_proxy_async_shared();  // generic smem use (routing) before bulk copies into it
             __syncthreads();
             stamp(p, 4);
-            if (cs->bcast[1]) gather_role(p, cs, flag, w);
+            if (cs->bcast[1]) gather_role(p, cs, w);
             __syncthreads();
             stamp(p, 5);
         }
@@ -2105,8 +2285,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (cs->bcast[2]) {
             stamp(p, 6);
             if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, true, flag, w);
-            else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), !p.direct, flag, w);
-            else compute_role<false>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), !p.direct, flag, w);
+            else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, &tmY, cs, whole_queue(p, cs), !p.direct, flag, w);
+            else compute_role<false>(p, &tmA, &tmB, &tmB3, &tmY, cs, whole_queue(p, cs), !p.direct, flag, w);
             stamp(p, 7);
         }
     }
@@ -2227,8 +2407,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int e0 = rank * epr, e1 = e0 + epr;
             const WorkQueue wq{&me->next_item, cs->item_start[e0], cs->item_start[e1], cs->offs[e0],
                                p.ep_ready[rank], cs->tile_start[e0]};
-            if (p.wide) compute_role<true>(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
-            else compute_role<false>(p, &maps.a[rank], &tmB, &tmB3, cs, wq, false, flag, w);
+            if (p.wide) compute_role<true>(p, &maps.a[rank], &tmB, &tmB3, nullptr, cs, wq, false, flag, w);
+            else compute_role<false>(p, &maps.a[rank], &tmB, &tmB3, nullptr, cs, wq, false, flag, w);
             stamp(p, 7);
         }
         if (p.combine_out) {
@@ -2302,7 +2482,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_combine_kernel(const Params p)
 template <int PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mk_gemm_kernel(const Params p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmB3) {
+                   const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmY) {
     CtrlSmem* cs = ctrl();
     const uint32_t flag = 1u;
     const WaitCtx w{&p.ctl->abort, flag, p.spin_limit_ns};
@@ -2317,8 +2497,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     build_tables(p, cs);
     __syncthreads();
     if constexpr (PAIR) compute_role_pair(p, &tmA, &tmB, cs, false, flag, w);
-    else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), false, flag, w);
-    else compute_role<false>(p, &tmA, &tmB, &tmB3, cs, whole_queue(p, cs), false, flag, w);
+    else if (p.wide) compute_role<true>(p, &tmA, &tmB, &tmB3, &tmY, cs, whole_queue(p, cs), false, flag, w);
+    else compute_role<false>(p, &tmA, &tmB, &tmB3, &tmY, cs, whole_queue(p, cs), false, flag, w);
     cta_teardown<PAIR>(p, cs, true);
 }
 
@@ -2329,8 +2509,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // clusters of two; if the driver refuses the cooperative attribute together
 // with clusters, it is launched without it after an occupancy check that
 // every cluster fits at once.
-cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, int grid,
-                         cudaStream_t st) {
+cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                         const CUtensorMap& y, int grid, cudaStream_t st) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NTHREADS);
@@ -2342,14 +2522,14 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
     cfg.attrs = attr;
     if (!p.pair) {
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, mk_fused_kernel<0>, p, a, b, b3);
+        return cudaLaunchKernelEx(&cfg, mk_fused_kernel<0>, p, a, b, b3, y);
     }
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 2;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3, y);
     if (err == cudaSuccess) return err;
     (void)cudaGetLastError();
     cfg.attrs = attr + 1;
@@ -2357,7 +2537,7 @@ cudaError_t launch_fused(const Params& p, const CUtensorMap& a, const CUtensorMa
     int clusters = 0;
     if ((err = cudaOccupancyMaxActiveClusters(&clusters, mk_fused_kernel<1>, &cfg)) != cudaSuccess) return err;
     if (2 * clusters < grid) return cudaErrorCooperativeLaunchTooLarge;
-    return cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3);
+    return cudaLaunchKernelEx(&cfg, mk_fused_kernel<1>, p, a, b, b3, y);
 }
 
 cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& b, const CUtensorMap& b3, int grid,
@@ -2378,7 +2558,7 @@ cudaError_t launch_ep(const Params& p, const CUtensorMap* a, const CUtensorMap& 
 }
 
 cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
-                           int grid, cudaStream_t st) {
+                           const CUtensorMap& y, int grid, cudaStream_t st) {
     mk_route_kernel<<<p.nch, NTHREADS, SMEM_BYTES, st>>>(p);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
@@ -2387,7 +2567,7 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     mk_gather_kernel<<<p.nch, NTHREADS, SMEM_BYTES, st>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (!p.pair) {
-        mk_gemm_kernel<0><<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b, b3);
+        mk_gemm_kernel<0><<<grid, NTHREADS, SMEM_BYTES, st>>>(p, a, b, b3, y);
         if ((err = cudaGetLastError()) != cudaSuccess || !p.combine_out) return err;
         mk_combine_kernel<<<grid, NTHREADS, COMBINE_SMEM + 1024, st>>>(p);
         return cudaGetLastError();
@@ -2404,7 +2584,7 @@ cudaError_t launch_unfused(const Params& p, const CUtensorMap& a, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((err = cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b, b3)) != cudaSuccess || !p.combine_out) return err;
+    if ((err = cudaLaunchKernelEx(&cfg, mk_gemm_kernel<1>, p, a, b, b3, y)) != cudaSuccess || !p.combine_out) return err;
     mk_combine_kernel<<<grid, NTHREADS, COMBINE_SMEM + 1024, st>>>(p);
     return cudaGetLastError();
 }

@@ -164,3 +164,18 @@ def test_reference_arm_on_a_reduced_case():
     d = json.loads([ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")][0])
     assert d["config"]["workload"].startswith("fine_grained_skewed_experts_div_8(T=1024,H=7168,F=2048,E=32,k=8")
     assert d["config"]["E"] == 32 and d["config"]["T"] == 1024 and d["value"] > 0
+
+
+def test_reduced_hidden_keeps_the_routing():
+    """`--h-div` shrinks only H: the logits, hence every expert's rows, are
+    those of the full layer (the skewed layer keeps its 40 active experts)."""
+    import numpy as np
+    import pytest
+
+    w = bench.synth.WORKLOADS[3]
+    r = bench.reduced_hidden(w, 8)
+    assert (r.T, r.E, r.k, r.F, r.seed, r.kind) == (w.T, w.E, w.k, w.F, w.seed, w.kind) and r.H == w.H // 8
+    assert np.array_equal(bench.synth.make_logits(r), bench.synth.make_logits(w))
+    assert bench.reduced_hidden(w, 1) is w
+    with pytest.raises(SystemExit):
+        bench.reduced_hidden(bench.synth.WORKLOADS[1], 16)  # 512 / 16 = 32: not a multiple of 64

@@ -101,12 +101,13 @@ def test_split_routing_special_logits(orc, kind, E, T):
 
 @pytest.mark.parametrize("E,T,grid,lanes", [
     (256, 128, 0, 8),      # decode-sized: 5 chunks of 28 tokens
-    (256, 8192, 0, 1),     # 4 lanes: 147 x 256 counts exceed the scan's 20480
-    (256, 2048, 0, 8),     # 74 chunks of 28 tokens (18944 counts)
-    (256, 4099, 0, 4),     # 8 lanes: 147 chunks, too many counts; 4 lanes: 74 chunks
+    (256, 8192, 0, 4),     # 8 lanes: 293 chunks; 4 lanes: 147 chunks of 56 (37632 counts, scanned by columns)
+    (256, 2048, 0, 8),     # 74 chunks of 28 tokens (18944 counts, scanned by columns)
+    (256, 4099, 0, 8),     # 147 chunks of 28 tokens
     (128, 16384, 0, 2),    # 147 chunks of 112 tokens
     (64, 4096, 0, 2),
     (8, 4096, 0, 1),       # other expert counts keep a lane per token
+    (8, 120000, 0, 1),     # 536 chunks, 3 or 4 per CTA: 4288 counts, scanned by columns
     (96, 500, 0, 1),
     (256, 1000, 8, 1),     # 8 CTAs: even two lanes give more chunks than CTAs
     (256, 1000, 10, 1),    # two lanes would fit 10 CTAs, but a lane scans at most 64 experts

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -148,17 +149,32 @@ int grid_for(const DevInfo& d, const mk_config_t& c) {
 
 // Role split from the shapes: the dispatch role gets the gather's share of
 // the path's estimated time (row bytes moved at HBM rate vs. the FLOPs at
-// tensor rate), at least an eighth of the grid and at most half of it.
-// Dispatch CTAs join the compute role once the gather queue is empty, so the
-// gather's total CTA time is the same for any split; a larger one fills the
-// first tiles sooner.  Measured on GB300 (Mixtral-like layer): 7 dispatch
-// CTAs 0.655 ms, 12: 0.642, 19 to 56: 0.638.
-int dispatch_split(int grid, int T, int H, int F, int k) {
+// tensor rate), and at least as many CTAs as the first wave of work items
+// (one per compute CTA) needs gather units, for evenly loaded experts, so
+// that every unit of those tiles is taken in the gather's first round; at
+// most half of the grid.  Dispatch CTAs join the compute role once the
+// gather queue is empty, so the gather's total CTA time is the same for any
+// split; a larger one fills the first tiles sooner.  (One SM's bulk copies
+// from HBM run at about 33 GB/s, so the gather's rate grows with its CTAs.)
+// The gather's share of the path's estimated time, in CTAs of the grid.
+int gather_share(int grid, int T, int H, int F, int k) {
     const double rows = double(T) * k;
     const double gather_s = rows * H * 4.0 / 6.0e12;
     const double gemm_s = 2.0 * rows * H * double(F) / 1.8e15;
-    int d = int(std::ceil(grid * gather_s / (gather_s + gemm_s)));
-    if (d < (grid + 7) / 8) d = (grid + 7) / 8;
+    return int(std::ceil(grid * gather_s / (gather_s + gemm_s)));
+}
+
+int dispatch_split(int grid, int T, int H, int F, int E, int k, int tile_rows, int nb, int slots) {
+    const double rows = double(T) * k;
+    int d = gather_share(grid, T, H, F, k);
+    // gather units of the tiles the first `grid` work items use
+    const double rows_e = rows / E;
+    const double tiles_e = std::ceil(rows_e / tile_rows);
+    const double items_e = tiles_e * nb;
+    const double experts_first = std::min(double(E), std::ceil(grid / std::max(items_e, 1.0)));
+    const double units_first =
+        experts_first * tiles_e * std::ceil(std::min(double(tile_rows), rows_e) / std::max(slots, 1));
+    if (d < units_first) d = int(units_first);
     if (d < 4) d = 4;
     if (d > grid / 2) d = grid / 2;
     if (d < 1) d = 1;
@@ -387,12 +403,19 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.compute = c.mode != MK_MODE_DISPATCH_ONLY;
     p.direct = direct ? 1 : 0;
     p.gather4 = gather4 ? 1 : 0;
+    {
+        int slots = int((SM_STAGE_END) / (size_t(H) * 2));
+        p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
+    }
     if (c.mode == MK_MODE_DISPATCH_ONLY) {
         p.dispatch_ctas = grid;
     } else if (direct) {
         p.dispatch_ctas = 0;  // rows go straight into the GEMM's shared memory: no gather role
     } else {
-        p.dispatch_ctas = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
+        p.dispatch_ctas = c.dispatch_ctas > 0 ? c.dispatch_ctas
+                                              : dispatch_split(grid, T, H, F, E, k, pair ? PAIR_TILE_M
+                                                                                       : wide ? WIDE_TILE_M : BM,
+                                                               p.nb, p.gather_slots);
         if (p.dispatch_ctas > grid) p.dispatch_ctas = grid;
         if (pair) p.dispatch_ctas = (p.dispatch_ctas + 1) & ~1;  // both CTAs of a cluster share a role
         if (p.dispatch_ctas > grid) p.dispatch_ctas = grid;
@@ -400,10 +423,6 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     p.pair = pair ? 1 : 0;
     p.wide = wide ? 1 : 0;
     p.tile_rows = pair ? PAIR_TILE_M : wide ? WIDE_TILE_M : BM;
-    {
-        int slots = int((SM_STAGE_END) / (size_t(H) * 2));
-        p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
-    }
     p.debug_drop_tile = c.debug_fault == MK_FAULT_DROP_TILE_FLAG ? 0 : -1;
     // measured on GB300: issuing L2 prefetches from the producer thread slows
     // the loads behind them, so it is off unless asked for
@@ -606,7 +625,7 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
         // role must be quick: about 64 sending CTAs in all (at most half of a
         // rank's) measured best or near it on GB300 for R = 2..8; they join
         // the GEMM once their rows are out.
-        int want = c.dispatch_ctas > 0 ? c.dispatch_ctas : dispatch_split(grid, T, H, F, k);
+        int want = c.dispatch_ctas > 0 ? c.dispatch_ctas : std::max(4, std::min(grid / 2, gather_share(grid, T, H, F, k)));
         if (c.dispatch_ctas <= 0 && ranks > 1 && want < 64) want = 64;
         int per = (want + ranks - 1) / ranks;
         if (c.dispatch_ctas <= 0 && ranks > 1 && per > cpr / 2) per = cpr / 2;

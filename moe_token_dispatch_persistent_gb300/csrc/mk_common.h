@@ -51,6 +51,9 @@ constexpr int SM_PB = SM_PA + PSTAGES * PA_STAGE_BYTES;    // 96 KiB
 // slower on GB300: per row of K the MMA warp waited longer, not shorter.)
 constexpr int WIDE_TILE_M = 2 * BM;
 constexpr int WSTAGES = 3;
+// Two-accumulator items issue their last K-block's MMAs accumulator by
+// accumulator, so the epilogue drains the first while the second finishes.
+constexpr bool WIDE_EARLY_HALF = true;
 
 constexpr int MAX_STAGES = PSTAGES > STAGES ? (PSTAGES > WSTAGES ? PSTAGES : WSTAGES)
                                              : (STAGES > WSTAGES ? STAGES : WSTAGES);
@@ -65,6 +68,9 @@ constexpr int EPI_BOX_COLS = 64;
 constexpr int EPI_BOX_ROWS = 32;
 constexpr int EPI_BUF_BYTES = EPI_BOX_COLS * EPI_BOX_ROWS * 2;
 constexpr int SM_EPI = SM_STAGE_END;
+// Whole boxes leave the buffer by one TMA store (true) or by coalesced
+// 16-byte stores of the warp after a transpose in the buffer (false).
+constexpr bool EPI_TMA_STORE = true;
 constexpr int SM_CTRL = SM_EPI + 4 * EPI_BUF_BYTES;           // 208 KiB
 constexpr int SM_CTRL_BYTES = 8192;
 constexpr int SMEM_BYTES = SM_CTRL + SM_CTRL_BYTES + 1024;    // + alignment slack

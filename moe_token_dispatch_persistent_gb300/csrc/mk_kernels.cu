@@ -774,19 +774,43 @@ __device__ __forceinline__ int find_expert(const int32_t* starts, int E, int v) 
 // row per slot lane, so several dispatch CTAs fill a tile at once and its
 // first items start soon after the scan.  Each lane moves its row
 // x[src] -> smem -> xs[row] with bulk copies and closes one bulk group per
-// unit (empty when it had no row).  A CTA's first unit is published as soon
-// as its stores complete (the first tiles gate the GEMM's start); after
-// that a unit's stores are waited for one unit later, while the next unit's
-// loads are in flight.  Publishing adds the unit's rows to the tile's
-// arrival count (release); the unit that completes a tile also counts it in
-// tiles_done.
+// unit (empty when it had no row).  The loop is software-pipelined: while a
+// unit's loads are in flight the next unit is claimed and its sources are
+// read.  Units of the tiles that the first wave of work items needs (items
+// [0, grid)) are published as soon as their stores complete: those tiles
+// gate the GEMM's start.  Later units are published one unit behind, their
+// stores completing while the next unit's loads are in flight.  Publishing
+// adds the unit's rows to the tile's arrival count (release); the unit that
+// completes a tile also counts it in tiles_done.
 __device__ __forceinline__ void publish_unit(const Params& p, int tile, int n, int trows) {
     if (tile == p.debug_drop_tile) return;  // host-side fault injection: this tile never completes
-    __threadfence();
+    // the release orders this thread's earlier writes (and, through the
+    // proxy fence the caller executed, the completed bulk stores) before it
     const uint32_t before = atom_add_acq_rel_u32(p.ready + tile, uint32_t(n));
     // once tiles_done reaches the tile count, one acquire of it stands in for
     // every tile's arrival count
     if (before + uint32_t(n) == uint32_t(trows)) atom_add_acq_rel_u32(&p.ctl->tiles_done, 1u);
+}
+
+__device__ __forceinline__ void decode_item(const Params& p, const CtrlSmem* cs, int item, Info& inf, int& gtile);
+
+// Geometry of gather unit u and the source token of this lane's row in it.
+struct GatherUnit {
+    int tile, row, n, trows, src_t;  // tile; this lane's sorted row; rows in the unit; rows in the tile
+};
+
+__device__ __forceinline__ GatherUnit gather_unit(const Params& p, const CtrlSmem* cs, int u, int unit, int upt,
+                                                  int lane) {
+    GatherUnit g{-1, 0, 0, 0, -1};
+    g.tile = u / upt;
+    const int e = find_expert(cs->tile_start, p.E, g.tile);
+    const int row0 = cs->offs[e] + (g.tile - cs->tile_start[e]) * p.tile_rows;
+    g.trows = min(p.tile_rows, cs->offs[e + 1] - row0);
+    const int r0 = (u - g.tile * upt) * unit;
+    g.n = max(0, min(unit, g.trows - r0));
+    g.row = row0 + r0 + lane;
+    if (lane < g.n) g.src_t = __ldcg(p.src_index + g.row) / p.k;
+    return g;
 }
 
 __device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
@@ -798,66 +822,85 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
     const int upt = (p.tile_rows + unit - 1) / unit;  // units per tile
     const int nunits = cs->tile_start[p.E] * upt;
     uint8_t* slot = s + size_t(lane) * row_bytes;
+    // tiles [0, urgent] hold the rows of the first wave of work items
+    int urgent = -1;
+    {
+        const int nfirst = min(int(gridDim.x), cs->item_start[p.E]);
+        for (int i = lane; i < nfirst; i += 32) {
+            Info inf;
+            int gt;
+            decode_item(p, cs, i, inf, gt);
+            urgent = max(urgent, gt);
+        }
+        urgent = __reduce_max_sync(0xffffffffu, urgent);
+    }
     uint32_t ph = 0;
-    bool ok = true, first = true;
+    bool ok = true;
     int pend_tile = -1, pend_n = 0, pend_rows = 0;    // the unit whose stores may still be in flight
+    int u = 0;
+    if (lane == 0) u = int(atom_add_relaxed_u32(&p.ctl->next_tile, 1u));
+    u = __shfl_sync(0xffffffffu, u, 0);
+    GatherUnit cur{-1, 0, 0, 0, -1};
+    if (u < nunits) cur = gather_unit(p, cs, u, unit, upt, lane);
     for (;;) {
-        int u = 0;
-        if (lane == 0) u = int(atom_add_relaxed_u32(&p.ctl->next_tile, 1u));
-        u = __shfl_sync(0xffffffffu, u, 0);
         const bool have = ok && u < nunits && !aborted(w);
-        int tile = -1, n = 0, trows = 0;
-        if (have) {
-            tile = u / upt;
-            const int e = find_expert(cs->tile_start, p.E, tile);
-            const int row0 = cs->offs[e] + (tile - cs->tile_start[e]) * p.tile_rows;
-            trows = min(p.tile_rows, cs->offs[e + 1] - row0);
-            const int r0 = (u - tile * upt) * unit;
-            n = max(0, min(unit, trows - r0));
-            if (lane < n) {
-                const int r = row0 + r0 + lane;
-                const int src_t = __ldcg(p.src_index + r) / p.k;
-                if (src_t < 0 || src_t >= p.T) {
-                    record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(r));
-                    raise_abort(w);
-                    ok = false;
-                } else {
-                    bulk_wait_read<0>();  // the slot's previous store has read it
-                    mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
-                    bulk_load(slot, p.x + size_t(src_t) * p.H, row_bytes, &cs->gbar[lane]);
-                    if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
-                        ok = false;
-                        // the load is in flight: give it a short, bounded chance to land
-                        WaitCtx shortw{nullptr, 0u, 2000000LL};
-                        wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
-                    }
-                    ph ^= 1u;
-                    if (ok) bulk_store(p.xs + size_t(r) * p.H, slot, row_bytes);
-                }
+        // claim the next unit now: its atomic and source reads overlap this unit's copies
+        int un = 0;
+        if (have && lane == 0) un = int(atom_add_relaxed_u32(&p.ctl->next_tile, 1u));
+        bool issued = false;
+        if (have && lane < cur.n) {
+            if (cur.src_t < 0 || cur.src_t >= p.T) {
+                record_error(ERR_FAULT, SITE_DEST_RANGE, uint32_t(cur.row));
+                raise_abort(w);
+                ok = false;
+            } else {
+                bulk_wait_read<0>();  // the slot's previous store has read it
+                mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
+                bulk_load(slot, p.x + size_t(cur.src_t) * p.H, row_bytes, &cs->gbar[lane]);
+                issued = true;
             }
+        }
+        un = __shfl_sync(0xffffffffu, un, 0);
+        GatherUnit nxt{-1, 0, 0, 0, -1};
+        if (have && un < nunits) nxt = gather_unit(p, cs, un, unit, upt, lane);
+        if (issued) {
+            if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
+                ok = false;
+                // the load is in flight: give it a short, bounded chance to land
+                WaitCtx shortw{nullptr, 0u, 2000000LL};
+                wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
+            }
+            ph ^= 1u;
+            if (ok) bulk_store(p.xs + size_t(cur.row) * p.H, slot, row_bytes);
         }
         bulk_commit();  // this unit's group (empty without a row)
         ok = __all_sync(0xffffffffu, ok);
-        if (first && have && n > 0) {
-            // the CTA's first unit: publish it without waiting for the next
+        if (have && cur.n > 0 && cur.tile <= urgent) {
+            // a unit of the first wave's tiles: publish it without waiting for
+            // the next one (and the one before it, if still pending)
             bulk_wait<0>();
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0 && ok) publish_unit(p, tile, n, trows);
-            first = false;
-            continue;
+            if (lane == 0 && ok) {
+                if (pend_tile >= 0) publish_unit(p, pend_tile, pend_n, pend_rows);
+                publish_unit(p, cur.tile, cur.n, cur.trows);
+            }
+            pend_tile = -1;
+        } else {
+            if (pend_tile >= 0) {
+                // the previous unit's group is complete once at most this one is pending
+                bulk_wait<1>();
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0 && ok) publish_unit(p, pend_tile, pend_n, pend_rows);
+            }
+            pend_tile = (have && cur.n > 0) ? cur.tile : -1;
+            pend_n = cur.n;
+            pend_rows = cur.trows;
         }
-        if (pend_tile >= 0) {
-            // the previous unit's group is complete once at most this one is pending
-            bulk_wait<1>();
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0 && ok) publish_unit(p, pend_tile, pend_n, pend_rows);
-        }
-        pend_tile = (have && n > 0) ? tile : -1;
-        pend_n = n;
-        pend_rows = trows;
         if (!have) break;
+        u = un;
+        cur = nxt;
     }
     bulk_wait_all();
 }
@@ -1071,15 +1114,17 @@ struct StageGeo {
 __device__ __forceinline__ uint64_t a_desc(uint32_t addr) { return umma_desc_sw128(addr, 16, 1024); }
 
 // Epilogue of 32 whole rows (TMEM lanes of this warp, all inside the tile)
-// through shared memory and tensor stores.  Per 64-column chunk the warp
-// reads its accumulator columns (for the gated FFN: the W1 and W3 halves,
-// SwiGLU applied), rounds them to bf16 and writes its 32 rows into its own
-// 4 KiB buffer in the 128-byte swizzle (lane = row, chunk c of row r at
-// r*128 + ((c ^ (r % 8)) * 16): conflict-free), and one lane stores the
-// 32 x 64 box with one TMA store.  A buffer is rewritten only after the
-// previous store has read it.  Each row's 32 stores of 32 bytes per item
-// (one per lane and instruction, 32 rows apart) become whole 128-byte lines.
-__device__ __forceinline__ void epi_rows_tma(const Params& p, const CUtensorMap* tmY, uint8_t* buf, uint32_t tbase,
+// through shared memory.  Per 64-column chunk the warp reads its
+// accumulator columns (for the gated FFN: the W1 and W3 halves, SwiGLU
+// applied), rounds them to bf16 and writes its 32 rows into its own 4 KiB
+// buffer in the 128-byte swizzle (lane = row, chunk c of row r at
+// r*128 + ((c ^ (r % 8)) * 16): conflict-free).  With EPI_TMA_STORE one lane
+// stores the 32 x 64 box with one TMA store (the buffer is rewritten once
+// that store has read it); otherwise the warp reads the box back with 8
+// lanes per row and writes four whole 128-byte lines per store
+// instruction.  Either way the per-row stores of the plain epilogue (32
+// rows, 32 bytes each, per warp instruction) become whole lines.
+__device__ __forceinline__ void epi_rows_box(const Params& p, const CUtensorMap* tmY, uint8_t* buf, uint32_t tbase,
                                              int n0, int row_first) {
     const int lane = threadIdx.x & 31;
     const int nchunks = (p.gated ? GATED_BN : BN) / EPI_BOX_COLS;
@@ -1119,18 +1164,40 @@ __device__ __forceinline__ void epi_rows_tma(const Params& p, const CUtensorMap*
                 pk[16 + u] = *reinterpret_cast<const uint32_t*>(&b1);
             }
         }
-        if (lane == 0) bulk_wait_read<0>();  // the previous box has left the buffer
-        __syncwarp();
         const uint32_t rowaddr = smem_u32(buf) + uint32_t(lane) * 128u;
+        if constexpr (EPI_TMA_STORE) {
+            if (lane == 0) bulk_wait_read<0>();  // the previous box has left the buffer
+            __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-            st_shared_v4(rowaddr + ((uint32_t(c) ^ uint32_t(lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                         pk[4 * c + 3]);
-        fence_proxy_async_shared();  // the generic writes before the tensor store reads them
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(tmY, buf, col, row_first);
-            bulk_commit();
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(rowaddr + ((uint32_t(c) ^ uint32_t(lane & 7)) << 4), pk[4 * c], pk[4 * c + 1],
+                             pk[4 * c + 2], pk[4 * c + 3]);
+            fence_proxy_async_shared();  // the generic writes before the tensor store reads them
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tmY, buf, col, row_first);
+                bulk_commit();
+            }
+        } else {
+            // transpose through the buffer: lane = row on the way in; on the way
+            // out 8 lanes cover one row's 128 bytes, so a warp store writes four
+            // whole lines
+            __syncwarp();  // the previous box has been read out of the buffer
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(rowaddr + ((uint32_t(c) ^ uint32_t(lane & 7)) << 4), pk[4 * c], pk[4 * c + 1],
+                             pk[4 * c + 2], pk[4 * c + 3]);
+            __syncwarp();
+            const int c = lane & 7, rq = lane >> 3;
+            uint16_t* ybase = static_cast<uint16_t*>(p.y) + size_t(row_first) * p.F + col + c * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + rq;  // r % 8 = rq + 4 * (i & 1)
+                uint32_t v0, v1, v2, v3;
+                ld_shared_v4(smem_u32(buf) + uint32_t(r) * 128u + ((uint32_t(c) ^ uint32_t(r & 7)) << 4), v0, v1, v2,
+                             v3);
+                *reinterpret_cast<uint4*>(ybase + size_t(r) * p.F) = make_uint4(v0, v1, v2, v3);
+            }
         }
     }
 }
@@ -1594,8 +1661,20 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     // A.W3 in [128, 256).
                     const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, G::BCH, 1024);
                     tc_mma_f16_elect(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    if (two)  // the second A block against the same B chunk
+                    if (two && !(WIDE_EARLY_HALF && kb == kblocks - 1))  // the second A block, same B chunk
                         tc_mma_f16_elect(d + BN, a_desc(a0 + G::ABLK + kk * 32), bd, IDESC,
+                                         (kb | kk) != 0 ? 1u : 0u);
+                }
+                if (WIDE_EARLY_HALF && two && kb == kblocks - 1) {
+                    // last K-block of a two-accumulator item: the first
+                    // accumulator's MMAs are all issued, so its epilogue may
+                    // start (acc_full[1], unused by wide tiles otherwise) while
+                    // the tensor core runs the second accumulator's last MMAs
+                    tc_commit_elect(&cs->acc_full[1]);
+#pragma unroll
+                    for (int kk = 0; kk < G::KB / 16; ++kk)
+                        tc_mma_f16_elect(d + BN, a_desc(a0 + G::ABLK + kk * 32),
+                                         umma_desc_sw128(b0 + kk * 2048, G::BCH, 1024), IDESC,
                                          (kb | kk) != 0 ? 1u : 0u);
                 }
                 issued = true;
@@ -1622,19 +1701,34 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
     } else if (warp < EPI_WARP_END) {
         // ---------------- epilogue: warps 2..5 ----------------
         const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32)
-        uint32_t acc = 0, accph = 0;
-        for (uint32_t it = 0;; ++it) {
+        uint32_t acc = 0, accph = 0, h0ph = 0;
+        bool ok = true;
+        for (uint32_t it = 0; ok; ++it) {
             const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
             if (!wait_mbar(&cs->info_full[slot], iph, wp, SITE_INFO_FULL)) break;
             const Info inf = cs->info[slot];
             __syncwarp();
             if (lane == 0) mbar_arrive(&cs->info_empty[slot]);
             if (inf.e < 0) break;
-            if (!wait_mbar(&cs->acc_full[acc], accph, wp, SITE_ACC_FULL)) break;
-            tc_fence_after();
             // WIDE: the tile's second 128 rows come from the second accumulator
             const int halves = (WIDE && inf.nrows > BM) ? 2 : 1;
+            // with two accumulators the first may be drained before the second is done
+            const bool early = WIDE_EARLY_HALF && halves == 2;
+            if (early) {
+                if (!wait_mbar(&cs->acc_full[1], h0ph, wp, SITE_ACC_FULL)) break;
+                h0ph ^= 1u;
+            } else if (!wait_mbar(&cs->acc_full[acc], accph, wp, SITE_ACC_FULL)) {
+                break;
+            }
+            tc_fence_after();
             for (int half = 0; half < halves; ++half) {
+                if (early && half == 1) {
+                    if (!wait_mbar(&cs->acc_full[acc], accph, wp, SITE_ACC_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
                 const int rloc = half * BM + quad * 32 + lane;
                 const bool rowok = rloc < inf.nrows;
                 // expert parallel: the result goes back to the sending rank, into
@@ -1644,7 +1738,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 const uint32_t tbase = cs->tmem_base + (uint32_t(quad * 32) << 16) + (acc + half) * BN;
                 if (tmY != nullptr && p.y_tma && half * BM + quad * 32 + 32 <= inf.nrows) {
                     // all 32 rows of this warp lie in the tile: tensor stores
-                    epi_rows_tma(p, tmY, s + SM_EPI + (warp - 2) * EPI_BUF_BYTES, tbase,
+                    epi_rows_box(p, tmY, s + SM_EPI + (warp - 2) * EPI_BUF_BYTES, tbase,
                                  inf.nbk * (p.gated ? GATED_BN : BN), inf.row0 + half * BM + quad * 32);
                 } else if (p.gated) {
                     const int n0 = inf.nbk * GATED_BN;
@@ -1706,6 +1800,7 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     }
                 }
             }
+            if (!ok) break;
             tc_fence_before();
             mbar_arrive(&cs->acc_empty[acc]);
             if (++acc == NACC) {
@@ -1716,8 +1811,10 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
         if (lane == 0) {
             // this warp's tensor stores have landed (visible to the combine
             // and to later kernels) before the role ends
-            bulk_wait_all();
-            fence_proxy_async();
+            if (EPI_TMA_STORE) {
+                bulk_wait_all();
+                fence_proxy_async();
+            }
         }
         __syncwarp();
     }

@@ -1623,7 +1623,14 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer: the whole warp runs the loop, one elected lane issues ----------------
-        uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
+        // WIDE: the epilogue frees the two accumulators one after the other
+        // (acc_empty[1]: rows 0-127 drained; acc_empty[0]: the whole tile).
+        // An item starts once the first is free; while the second is still
+        // being drained, its K-blocks run on the first accumulator alone, up
+        // to a full ring of stages, and the second accumulator's MMAs of those
+        // K-blocks follow, in order, once it is free.  Each accumulator still
+        // sums its K-blocks in ascending order, so results are unchanged.
+        uint32_t stage = 0, phase = 0, acc = 0, accph = 0, e0ph = 0;
         bool issued = false;
         for (uint32_t it = 0;; ++it) {
             const uint32_t slot = it & 3u, iph = (it >> 2) & 1u;
@@ -1633,11 +1640,19 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             __syncwarp();
             if (lane == 0) mbar_arrive(&cs->info_empty[slot]);
             if (e < 0) break;
-            if (!warp_wait_mbar(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
+            if (WIDE) {
+                if (!warp_wait_mbar(&cs->acc_empty[1], e0ph ^ 1u, wp, SITE_ACC_EMPTY)) break;
+                e0ph ^= 1u;
+            } else if (!warp_wait_mbar(&cs->acc_empty[acc], accph ^ 1u, wp, SITE_ACC_EMPTY)) {
+                break;
+            }
             tc_fence_after();
             // WIDE: rows 0-127 in TMEM columns [0, 256), rows 128-255 in [256, 512)
             const uint32_t d = cs->tmem_base + acc * BN;
             bool ok = true;
+            bool second_free = false;             // two: the second accumulator may be written
+            int kb_lo = 0;                        // two: first K-block without its second-accumulator MMAs
+            uint32_t st_lo = stage;               // ... and its stage
             for (int kb = 0; kb < kblocks; ++kb) {
                 if (!warp_wait_mbar(&cs->full[stage], phase, wp, SITE_STAGE_FULL)) {
                     ok = false;
@@ -1661,30 +1676,55 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                     // A.W3 in [128, 256).
                     const uint64_t bd = umma_desc_sw128(b0 + kk * 2048, G::BCH, 1024);
                     tc_mma_f16_elect(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    if (two && !(WIDE_EARLY_HALF && kb == kblocks - 1))  // the second A block, same B chunk
-                        tc_mma_f16_elect(d + BN, a_desc(a0 + G::ABLK + kk * 32), bd, IDESC,
-                                         (kb | kk) != 0 ? 1u : 0u);
-                }
-                if (WIDE_EARLY_HALF && two && kb == kblocks - 1) {
-                    // last K-block of a two-accumulator item: the first
-                    // accumulator's MMAs are all issued, so its epilogue may
-                    // start (acc_full[1], unused by wide tiles otherwise) while
-                    // the tensor core runs the second accumulator's last MMAs
-                    tc_commit_elect(&cs->acc_full[1]);
-#pragma unroll
-                    for (int kk = 0; kk < G::KB / 16; ++kk)
-                        tc_mma_f16_elect(d + BN, a_desc(a0 + G::ABLK + kk * 32),
-                                         umma_desc_sw128(b0 + kk * 2048, G::BCH, 1024), IDESC,
-                                         (kb | kk) != 0 ? 1u : 0u);
                 }
                 issued = true;
-                tc_commit_elect(&cs->empty[stage]);
+                if (two) {
+                    const bool last = kb == kblocks - 1;
+                    // last K-block: the first accumulator's MMAs are all issued,
+                    // so its epilogue may start (acc_full[1], unused by wide tiles
+                    // otherwise) while the tensor core runs the second's last MMAs
+                    if (WIDE_EARLY_HALF && last) tc_commit_elect(&cs->acc_full[1]);
+                    if (!second_free) {
+                        if (last || kb - kb_lo + 1 == NST) {
+                            // no stage left to run ahead on: wait for the second accumulator
+                            if (!warp_wait_mbar(&cs->acc_empty[0], accph ^ 1u, wp, SITE_ACC_EMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                            second_free = true;
+                        } else {
+                            second_free = __all_sync(0xffffffffu, mbar_try_wait(&cs->acc_empty[0], accph ^ 1u));
+                        }
+                        if (second_free) tc_fence_after();
+                    }
+                    if (second_free) {
+                        for (; kb_lo <= kb; ++kb_lo) {
+                            // the second A block of each K-block not yet issued, same B chunk
+                            const uint32_t a1 = smem_u32(s + SMA + st_lo * ASB) + G::ABLK;
+                            const uint32_t b1 = smem_u32(s + SMB + st_lo * G::BSB);
+#pragma unroll
+                            for (int kk = 0; kk < G::KB / 16; ++kk)
+                                tc_mma_f16_elect(d + BN, a_desc(a1 + kk * 32),
+                                                 umma_desc_sw128(b1 + kk * 2048, G::BCH, 1024), IDESC,
+                                                 (kb_lo | kk) != 0 ? 1u : 0u);
+                            tc_commit_elect(&cs->empty[st_lo]);
+                            if (++st_lo == NST) st_lo = 0;
+                        }
+                    }
+                } else {
+                    tc_commit_elect(&cs->empty[stage]);
+                }
                 if (++stage == NST) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
+            if (WIDE && !two) {
+                // one-accumulator item: keep in step with the epilogue's
+                // release of the second accumulator (long done by now)
+                if (!warp_wait_mbar(&cs->acc_empty[0], accph ^ 1u, wp, SITE_ACC_EMPTY)) break;
+            }
             tc_commit_elect(&cs->acc_full[acc]);
             if (++acc == NACC) {
                 acc = 0;
@@ -1798,6 +1838,11 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                             st_release_sys_u32(&p.stream_flag[c], p.stream_seq);
                         }
                     }
+                }
+                if (WIDE && half == 0) {
+                    // the first accumulator is drained: the next item's MMAs may start
+                    tc_fence_before();
+                    mbar_arrive(&cs->acc_empty[1]);
                 }
             }
             if (!ok) break;

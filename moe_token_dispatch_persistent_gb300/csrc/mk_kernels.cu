@@ -1558,46 +1558,11 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 cs->info[slot] = inf;
                 mbar_arrive(&cs->info_full[slot]);
             }
-            if (wq.arrived) {
-                // every source's rows of this tile have landed
-                if (!warp_wait_geq(wq.arrived + (gtile - wq.tile_lo), uint32_t(inf.nrows), w, SITE_TILE_READY)) {
-                    ok = false;
-                    break;
-                }
-                fence_proxy_async();
-            } else if (wait_ready) {
-                // one acquire per item until every tile is known to be in;
-                // before that, the tile's arrival count reaches its rows
-                if (__all_sync(0xffffffffu, ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles))) {
-                    wait_ready = false;
-                } else if (!warp_wait_geq(p.ready + gtile, uint32_t(inf.nrows), w, SITE_TILE_READY)) {
-                    ok = false;
-                    break;
-                }
-                fence_proxy_async();
-            }
             const int ncol = p.F;
-            const int kclaim = max(0, kblocks - CLAIM_LEAD);
-            for (int kb = 0; kb < kblocks; ++kb) {
-                if (kb == kclaim && lane == 0) ahead = atom_add_relaxed_u32(wq.next, 1u);
-                if (!warp_wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                if (pf > 0 && kb + pf < kblocks) {
-#pragma unroll
-                    for (int q = 0; q < BN / 64; ++q) {
-                        const int col = inf.nbk * BN + q * 64;
-                        if (col < ncol) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + (kb + pf) * G::KB);
-                    }
-                }
-                uint64_t* fb = &cs->full[stage];
-                const bool two = WIDE && inf.nrows > BM;  // second 128-row A block
-                mbar_arrive_expect_tx_elect(fb, (two ? 2 : 1) * G::ABLK + G::BSB);
-                uint8_t* a = s + SMA + stage * ASB;
-                uint8_t* b = s + SMB + stage * G::BSB;
-                tma_load_2d_elect(a, tmA, kb * G::KB, inf.row0 - wq.a_row0, fb);
-                if (two) tma_load_2d_elect(a + G::ABLK, tmA, kb * G::KB, inf.row0 - wq.a_row0 + BM, fb);
+            const bool two = WIDE && inf.nrows > BM;  // second 128-row A block
+            const uint32_t stage_bytes = (two ? 2 : 1) * G::ABLK + G::BSB;
+            // this item's weight boxes of K-block kb into B stage b
+            auto load_b = [&](int kb, uint8_t* b, uint64_t* fb) {
                 if (p.gated) {
                     // 128 columns of W1 into the first half of the B stage, of W3 into the second
 #pragma unroll
@@ -1616,6 +1581,59 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                                           fb);
                     }
                 }
+            };
+            // The CTA's first item finds every stage free: its first weight
+            // boxes (which do not depend on the gather) go out before the wait
+            // for the tile's rows, and the rows follow into the same stages.
+            int pre = 0;
+            if (it == 0 && (wq.arrived || wait_ready)) {
+                pre = min(NST, kblocks);
+                for (int kb = 0; kb < pre; ++kb) {
+                    mbar_arrive_expect_tx_elect(&cs->full[kb], stage_bytes);
+                    load_b(kb, s + SMB + kb * G::BSB, &cs->full[kb]);
+                    issued_any |= 1u << kb;  // stage kb, phase 0: the first use of every stage
+                }
+            }
+            if (wq.arrived) {
+                // every source's rows of this tile have landed
+                if (!warp_wait_geq(wq.arrived + (gtile - wq.tile_lo), uint32_t(inf.nrows), w, SITE_TILE_READY)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async();
+            } else if (wait_ready) {
+                // one acquire per item until every tile is known to be in;
+                // before that, the tile's arrival count reaches its rows
+                if (__all_sync(0xffffffffu, ld_acquire_u32(&p.ctl->tiles_done) >= uint32_t(ntiles))) {
+                    wait_ready = false;
+                } else if (!warp_wait_geq(p.ready + gtile, uint32_t(inf.nrows), w, SITE_TILE_READY)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async();
+            }
+            const int kclaim = max(0, kblocks - CLAIM_LEAD);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (kb == kclaim && lane == 0) ahead = atom_add_relaxed_u32(wq.next, 1u);
+                uint64_t* fb = &cs->full[stage];
+                if (kb >= pre) {
+                    if (!warp_wait_mbar(&cs->empty[stage], phase ^ 1u, wp, SITE_STAGE_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    if (pf > 0 && kb + pf < kblocks) {
+#pragma unroll
+                        for (int q = 0; q < BN / 64; ++q) {
+                            const int col = inf.nbk * BN + q * 64;
+                            if (col < ncol) tma_prefetch_l2_2d_elect(tmB, col, inf.e * p.H + (kb + pf) * G::KB);
+                        }
+                    }
+                    mbar_arrive_expect_tx_elect(fb, stage_bytes);
+                    load_b(kb, s + SMB + stage * G::BSB, fb);
+                }
+                uint8_t* a = s + SMA + stage * ASB;
+                tma_load_2d_elect(a, tmA, kb * G::KB, inf.row0 - wq.a_row0, fb);
+                if (two) tma_load_2d_elect(a + G::ABLK, tmA, kb * G::KB, inf.row0 - wq.a_row0 + BM, fb);
                 issued_any |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == NST) {

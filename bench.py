@@ -73,6 +73,9 @@ def parse_args(argv=None):
     ap.add_argument("--experts-div", type=int, default=1,
                     help="small case for profiler captures: E/D experts and T/D tokens, H, F, k and the value "
                          "recipe unchanged (not a bench workload)")
+    ap.add_argument("--trace", action="store_true",
+                    help="instead of the bench line: per-phase times of the fused launch (trace stamps, median of "
+                         "5 traced launches after 3 warm-ups) for each workload of --configs, one JSON line")
     ap.add_argument("--h-div", type=int, default=1,
                     help="small case for profiler captures: H/D, everything else unchanged, so routing and the "
                          "rows of every expert stay those of the full layer (not a bench workload)")
@@ -832,11 +835,71 @@ def run_ours(args, w):
     return 0
 
 
+TRACE_PHASES = {0: "cta_start", 1: "routing_done", 2: "routing_barrier", 3: "scatter_done", 4: "scatter_barrier",
+                5: "gather_done", 6: "gemm_start", 7: "gemm_end", 8: "combine_barrier", 9: "combine_done",
+                10: "first_mma", 11: "last_mma", 15: "cta_exit"}
+
+
+def run_trace(args):
+    """Phase timeline of the fused launch per workload: for each traced
+    stamp, the earliest, median and latest CTA in µs after the first CTA
+    started (medians over 5 traced launches), and the CTAs that reached it."""
+    g = Gpu(0)
+    mk, torch = g.mk, g.torch
+    wanted = [int(c) for c in args.configs.split(",") if c] if args.configs.strip().lower() != "none" else []
+    out_all = {}
+    for wid in wanted:
+        w = synth.WORKLOADS[wid]
+        ch = synth._streams(w)
+        x, logits, W = g.upload(synth.make_x(w, ch), synth.make_logits(w, ch), synth.make_w(w))
+        out = mk.alloc_outputs(w.T, w.F, w.E, w.k, device=g.dev)
+        mode = mk.MK_MODE_DISPATCH_ONLY if args.dispatch_only else mk.MK_MODE_FUSED
+        cfg = mk.make_config(mode=mode, trace=1)
+        runs = []
+        for rep in range(8):
+            g.flush.fill_(1)
+            st = mk.mk_moe_dispatch_gemm_ex(x, logits, w.T, w.H, w.E, w.k, W, w.F, out["y_sorted"], out["src_index"],
+                                            out["expert_offsets"], out["gate_w"], g.stream, cfg)
+            if st != mk.MK_OK:
+                raise mk.MkError(st, "mk_moe_dispatch_gemm_ex")
+            torch.cuda.synchronize()
+            info = mk.mk_last_launch_info()
+            tr = mk.mk_read_trace(w.T, w.H, w.E, w.k, info["grid_ctas"], stream=g.stream).astype(np.int64)
+            if rep < 3:
+                continue
+            t0 = tr[:, 0][tr[:, 0] > 0].min()
+            row = {}
+            for slot, name in TRACE_PHASES.items():
+                v = tr[:, slot]
+                v = (v[v > 0] - t0) / 1e3
+                if len(v):
+                    row[name] = [float(v.min()), float(np.median(v)), float(v.max()), int(len(v))]
+            runs.append(row)
+        st = mk.mk_get_status(g.stream)
+        if st != mk.MK_OK:
+            raise mk.MkError(st, "device status")
+        summary = {}
+        for name in TRACE_PHASES.values():
+            vals = [r[name] for r in runs if name in r]
+            if vals:
+                summary[name] = [round(float(np.median([v[i] for v in vals])), 1) for i in range(3)] + [vals[0][3]]
+        out_all[w.describe()] = {"dispatch_ctas": info["dispatch_ctas"], "grid_ctas": info["grid_ctas"],
+                                 "mode": "dispatch only" if args.dispatch_only else "fused", "phases_us": summary}
+        del x, logits, W, out
+        mk.mk_release_workspace()
+        torch.cuda.empty_cache()
+    print(json.dumps({"trace": out_all, "unit": "µs after the first CTA started: [earliest, median, latest CTA, CTAs]"}),
+          flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     w = reduced_hidden(reduced_workload(synth.WORKLOADS[args.config], args.experts_div), args.h_div)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.trace:
+        return run_trace(args)
     return run_ours(args, w)
 
 

@@ -307,7 +307,12 @@ void mk_last_launch_info(mk_launch_info_t* info);
  * these sizes on `stream` to the host: up to n uint64 values, 16 per CTA
  * (%globaltimer ns; 0 = phase not reached).  `workspace` is the caller
  * workspace that call used, or NULL for the library cache of `stream`.
- * Synchronises `stream`. */
+ * Synchronises `stream`.  Slots of the fused single-SM kernel: 0 CTA start,
+ * 1 its routing chunks done, 2 routing barrier passed, 3 scan and scatter
+ * done, 4 scatter barrier passed (dispatch CTAs), 5 gather done (dispatch
+ * CTAs), 6 GEMM role start, 7 GEMM role end, 8 combine barrier passed,
+ * 9 combine done, 10 first full stage reaches the tensor core, 11 last MMA
+ * completed, 15 CTA exit. */
 mk_status_t mk_read_trace(void* stream, const void* workspace, int T, int H, int E, int k, uint64_t* out,
                           size_t n);
 

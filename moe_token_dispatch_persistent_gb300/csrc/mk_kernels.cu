@@ -1698,6 +1698,8 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
                 // them before the tensor core reads the stage
                 if (p.direct && !p.gather4) fence_proxy_async_shared();
                 tc_fence_after();
+                // trace: this CTA's first full stage reaches the tensor core
+                if (!issued && p.trace && lane == 0) p.trace_buf[blockIdx.x * TRACE_SLOTS + 10] = globaltimer();
                 const uint32_t a0 = smem_u32(s + SMA + stage * ASB);
                 const uint32_t b0 = smem_u32(s + SMB + stage * G::BSB);
 #pragma unroll
@@ -1772,6 +1774,8 @@ __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUte
             tc_commit_elect(&cs->drain);
             WaitCtx shortw{nullptr, 0u, 5000000LL};
             warp_wait_mbar(&cs->drain, 0u, shortw, SITE_DRAIN);
+            // trace: this CTA's last MMA has completed
+            if (p.trace && lane == 0) p.trace_buf[blockIdx.x * TRACE_SLOTS + 11] = globaltimer();
         }
         __syncwarp();
     } else if (warp < EPI_WARP_END) {

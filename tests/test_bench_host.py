@@ -179,3 +179,11 @@ def test_reduced_hidden_keeps_the_routing():
     assert bench.reduced_hidden(w, 1) is w
     with pytest.raises(SystemExit):
         bench.reduced_hidden(bench.synth.WORKLOADS[1], 16)  # 512 / 16 = 32: not a multiple of 64
+
+
+def test_trace_mode_is_a_separate_output():
+    """--trace prints a phase timeline instead of the bench line; the default
+    run (what the driver launches) never traces."""
+    assert bench.parse_args(["--trace"]).trace is True
+    assert bench.parse_args([]).trace is False
+    assert bench.TRACE_PHASES[10] == "first_mma" and bench.TRACE_PHASES[15] == "cta_exit"

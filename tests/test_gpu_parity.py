@@ -226,6 +226,27 @@ def test_trace_records_phases():
     assert (tr[: info["dispatch_ctas"], 5] > 0).all()  # every dispatch CTA finished its gather
 
 
+@pytest.mark.parametrize("gather", [mk.MK_GATHER_STAGED, mk.MK_GATHER_DIRECT], ids=["staged", "direct"])
+@pytest.mark.parametrize("tiles", [mk.MK_MMA_SINGLE, mk.MK_MMA_WIDE], ids=["single", "wide"])
+def test_trace_phase_order(gather, tiles):
+    """Every CTA's stamps come in phase order: routing, its barrier, scan and
+    scatter, the GEMM role, its first full stage at the tensor core, its
+    last MMA, the exit.  (The role's end is stamped by the producer warp,
+    which may finish before the MMA warp's last MMAs complete.)"""
+    T, H, F, E, k = 3000, 512, 768, 16, 4
+    x, l, W = gu.to_device(*_inputs(T, H, F, E, k, seed=61))
+    mk.moe_dispatch_gemm(x, l, W, k, cfg=mk.make_config(trace=1, gather=gather, mma_pair=tiles))
+    info = mk.mk_last_launch_info()
+    tr = mk.mk_read_trace(T, H, E, k, info["grid_ctas"]).astype(np.int64)
+    for slot in (0, 1, 2, 3, 15):
+        assert (tr[:, slot] > 0).all(), slot
+    assert (tr[:, 1] >= tr[:, 0]).all() and (tr[:, 2] >= tr[:, 1]).all() and (tr[:, 3] >= tr[:, 2]).all()
+    gemm = tr[:, 10] > 0  # CTAs whose GEMM role issued at least one MMA
+    assert gemm.sum() > 0
+    assert (tr[gemm, 10] >= tr[gemm, 6]).all() and (tr[gemm, 11] >= tr[gemm, 10]).all()
+    assert (tr[gemm, 15] >= tr[gemm, 11]).all() and (tr[gemm, 7] >= tr[gemm, 6]).all()
+
+
 def test_two_streams_at_once():
     """Calls on two streams, enqueued back to back without synchronising:
     each stream has its own cached workspace and both results are right."""

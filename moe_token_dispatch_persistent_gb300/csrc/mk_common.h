@@ -50,6 +50,8 @@ constexpr int SM_PB = SM_PA + PSTAGES * PA_STAGE_BYTES;    // 96 KiB
 // (Six stages of 32 rows of K, the same bytes in finer steps, measured 17%
 // slower on GB300: per row of K the MMA warp waited longer, not shorter.)
 constexpr int WIDE_TILE_M = 2 * BM;
+static_assert((BM & (BM - 1)) == 0 && (WIDE_TILE_M & (WIDE_TILE_M - 1)) == 0 && (PAIR_TILE_M & (PAIR_TILE_M - 1)) == 0,
+              "tile rows are powers of two (the tile tables count tiles with a shift)");
 constexpr int WSTAGES = 3;
 // Two-accumulator items issue their last K-block's MMAs accumulator by
 // accumulator, so the epilogue drains the first while the second finishes.

@@ -108,7 +108,8 @@ typedef struct mk_config {
  * as DIRECT, but the rows arrive by TMA tile::gather4 (four token rows per
  * instruction, one instruction per lane of the producer warp) instead of
  * cp.async; same tiles and limits.  AUTO: DIRECT when k >= 4 and
- * T*k >= 256*E (wide tiles), with cfg.mma_pair AUTO or WIDE and
+ * T*k >= 256*E (wide tiles), or when the staged rows would take under
+ * 1 MiB (T*k*H*2 < 2^20), with cfg.mma_pair AUTO or WIDE and
  * T*H*2 < 4 GiB; STAGED otherwise.  The expert-parallel entry points stage
  * rows (DIRECT and GATHER4 return MK_ERR_UNSUPPORTED there). */
 enum { MK_GATHER_AUTO = 0, MK_GATHER_STAGED = 1, MK_GATHER_DIRECT = 2, MK_GATHER_GATHER4 = 3 };

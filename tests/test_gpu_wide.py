@@ -227,15 +227,18 @@ def test_wide_expert_parallel_bitwise(R):
     assert torch.equal(g["out"], single["out"])
 
 
-@pytest.mark.parametrize("T,E,k,tiles,gather", [
-    (4096, 8, 2, WIDE, mk.MK_GATHER_STAGED),          # Mixtral-like shape: wide, staged
-    (2048, 64, 8, WIDE, mk.MK_GATHER_DIRECT),          # fine-grained routing: wide, rows straight from x
-    (128, 256, 8, mk.MK_MMA_SINGLE, mk.MK_GATHER_STAGED),  # decode: 4 rows per expert
-    (1000, 64, 8, mk.MK_MMA_SINGLE, mk.MK_GATHER_STAGED),  # 125 rows per expert on average
+@pytest.mark.parametrize("T,E,k,H,tiles,gather", [
+    (4096, 8, 2, 64, WIDE, mk.MK_GATHER_STAGED),              # Mixtral-like shape: wide, staged (1 MiB of rows)
+    (2048, 64, 8, 64, WIDE, mk.MK_GATHER_DIRECT),              # fine-grained routing: wide, rows straight from x
+    (128, 256, 8, 64, mk.MK_MMA_SINGLE, mk.MK_GATHER_DIRECT),  # decode-shaped, under 1 MiB of rows
+    (1000, 64, 8, 64, mk.MK_MMA_SINGLE, mk.MK_GATHER_DIRECT),  # 125 rows per expert, under 1 MiB of rows
+    (2000, 64, 8, 64, mk.MK_MMA_SINGLE, mk.MK_GATHER_STAGED),  # 2 MiB of rows, not wide: staged
+    (128, 256, 8, 7168, mk.MK_MMA_SINGLE, mk.MK_GATHER_STAGED),  # decode layer: 15 MB of rows, staged
+    (256, 8, 2, 512, mk.MK_MMA_SINGLE, mk.MK_GATHER_DIRECT),   # the tiny layer: 0.5 MiB of rows
 ])
-def test_auto_resolution(T, E, k, tiles, gather):
+def test_auto_resolution(T, E, k, H, tiles, gather):
     """What AUTO picks, per shape (the reported launch facts)."""
-    H, F = 64, 64
+    F = 64
     xd, ld, Wd = gu.to_device(*_inputs(T, H, F, E, k, seed=31))
     mk.moe_dispatch_gemm(xd, ld, Wd, k)
     torch.cuda.synchronize()

@@ -76,7 +76,8 @@ enum { MK_OUT_BF16 = 0, MK_OUT_F32 = 1 };
 
 /* Host-side fault injection (never a device trap): withhold the arrival of
  * one tile's rows (its readiness never completes) so the compute role's
- * bounded wait runs out. */
+ * bounded wait runs out.  It acts on staged rows: with the fault set, AUTO
+ * row sources resolve to MK_GATHER_STAGED. */
 enum { MK_FAULT_NONE = 0, MK_FAULT_DROP_TILE_FLAG = 1 };
 
 typedef struct mk_config {

@@ -195,6 +195,8 @@ bool wide_shape(int T, int E, int k) { return int64_t(T) * k >= int64_t(2 * BM) 
 int resolve_gather(const mk_config_t& c, int T, int H, int E, int k) {
     if (c.mode == MK_MODE_DISPATCH_ONLY) return MK_GATHER_STAGED;
     if (c.gather != MK_GATHER_AUTO) return c.gather;
+    // the injected fault withholds a staged tile's arrival count
+    if (c.debug_fault != MK_FAULT_NONE) return MK_GATHER_STAGED;
     if (c.mma_pair == MK_MMA_PAIR || c.mma_pair == MK_MMA_SINGLE) return MK_GATHER_STAGED;
     const bool fits = uint64_t(T) * uint64_t(H) * 2 < (uint64_t(1) << 32);  // 32-bit row offsets into x
     // Under 1 MiB of rows to stage the gather is pure latency before the

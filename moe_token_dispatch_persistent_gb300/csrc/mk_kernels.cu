@@ -1499,9 +1499,10 @@ __device__ __forceinline__ int rank_of_token(const Params& p, int t) {
 // blocks and one B block; two 128 x 256 accumulators (all 512 TMEM columns)
 // share that B block, so a stage carries 64 KiB for 1024 cycles of MMA
 // instead of 48 KiB for 512.  With TMEM full, the accumulators are
-// single-buffered: the next item's MMAs wait until the epilogue has read
-// both.  A tile of at most 128 rows (an expert's last) uses one accumulator
-// and loads one A block.
+// single-buffered: the epilogue frees the first as soon as it has read it,
+// and the next item's MMAs start on that one while the second is read (see
+// the MMA issuer).  A tile of at most 128 rows (an expert's last) uses one
+// accumulator and loads one A block.
 template <bool WIDE>
 __device__ void compute_role(const Params& p, const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmB3,
                              const CUtensorMap* tmY, CtrlSmem* cs, const WorkQueue& wq,

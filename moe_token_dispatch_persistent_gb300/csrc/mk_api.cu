@@ -190,8 +190,9 @@ bool wide_shape(int T, int E, int k) { return int64_t(T) * k >= int64_t(2 * BM) 
 // workspace, no gather role).  Dispatch-only always stages (it measures the
 // gather).  AUTO: DIRECT for fine-grained routing (k >= 4) on wide tiles,
 // where staging would copy T*k rows of x (0.9-1.1 GB on the skewed and
-// imbalanced workloads) and direct rows measured 13-15% faster on GB300;
-// STAGED otherwise (the Mixtral-like layer, k = 2, runs 2% faster staged).
+// imbalanced workloads) and direct rows measured 13-15% faster on GB300,
+// and for problems with under 1 MiB of rows to stage; STAGED otherwise (the
+// Mixtral-like layer, k = 2, runs 6% faster staged).
 int resolve_gather(const mk_config_t& c, int T, int H, int E, int k) {
     if (c.mode == MK_MODE_DISPATCH_ONLY) return MK_GATHER_STAGED;
     if (c.gather != MK_GATHER_AUTO) return c.gather;
@@ -415,6 +416,9 @@ mk_status_t run_path(const void* x, const float* logits, int T, int H, int E, in
     {
         int slots = int((SM_STAGE_END) / (size_t(H) * 2));
         p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
+        // several gathering warps only where tiles are whole: with a few rows
+        // per expert (decode) smaller units would mostly be empty
+        p.gather_warps = wide_shape(T, E, k) ? std::min(GATHER_WARPS, p.gather_slots) : 1;
     }
     if (c.mode == MK_MODE_DISPATCH_ONLY) {
         p.dispatch_ctas = grid;
@@ -610,6 +614,7 @@ mk_status_t run_ep(const void* x, const float* logits, int T, int H, int E, int 
     {
         int slots = int((SM_STAGE_END) / (size_t(H) * 2));
         p.gather_slots = slots > MAX_GATHER_SLOTS ? MAX_GATHER_SLOTS : slots;
+        p.gather_warps = 1;  // the expert-parallel send role copies with one warp
     }
     p.debug_drop_tile = c.debug_fault == MK_FAULT_DROP_TILE_FLAG ? 0 : -1;
     p.spin_limit_ns = c.spin_limit_ns > 0 ? c.spin_limit_ns : kDefaultSpinNs;

@@ -772,9 +772,10 @@ __device__ __forceinline__ int find_expert(const int32_t* starts, int E, int v) 
     return lo;
 }
 
-// Dispatch role (warp 0): pull gather units from the queue in GEMM
-// consumption order.  A unit is up to `gather_slots` rows of one tile, one
-// row per slot lane, so several dispatch CTAs fill a tile at once and its
+// Dispatch role (the first p.gather_warps warps, each on its own share of
+// the slots): pull gather units from the queue in GEMM consumption order.
+// A unit is up to gather_slots / gather_warps rows of one tile, one row per
+// slot lane, so several dispatch CTAs fill a tile at once and its
 // first items start soon after the scan.  Each lane moves its row
 // x[src] -> smem -> xs[row] with bulk copies and closes one bulk group per
 // unit (empty when it had no row).  The loop is software-pipelined: while a
@@ -828,13 +829,15 @@ __device__ __forceinline__ GatherUnit gather_unit(const Params& p, const CtrlSme
 
 __device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp != 0) return;
+    const int gw = p.gather_warps;  // each gathering warp runs this loop on its own slots
+    if (warp >= gw) return;
     uint8_t* s = smem_base();
     const uint32_t row_bytes = uint32_t(p.H) * 2u;
-    const int unit = p.gather_slots;                  // rows per unit: one per slot lane
+    const int unit = p.gather_slots / gw;             // rows per unit: one per slot lane
     const int upt = (p.tile_rows + unit - 1) / unit;  // units per tile
     const int nunits = cs->tile_start[p.E] * upt;
-    uint8_t* slot = s + size_t(lane) * row_bytes;
+    const int sl = min(warp * unit + lane, p.gather_slots - 1);  // this lane's slot (lanes >= unit never copy)
+    uint8_t* slot = s + size_t(sl) * row_bytes;
     // tiles [0, urgent] hold the rows of the first wave of work items
     int urgent = -1;
     {
@@ -868,8 +871,8 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
                 ok = false;
             } else {
                 bulk_wait_read<0>();  // the slot's previous store has read it
-                mbar_arrive_expect_tx(&cs->gbar[lane], row_bytes);
-                bulk_load(slot, p.x + size_t(cur.src_t) * p.H, row_bytes, &cs->gbar[lane]);
+                mbar_arrive_expect_tx(&cs->gbar[sl], row_bytes);
+                bulk_load(slot, p.x + size_t(cur.src_t) * p.H, row_bytes, &cs->gbar[sl]);
                 issued = true;
             }
         }
@@ -877,11 +880,11 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
         GatherUnit nxt{-1, 0, 0, 0, -1};
         if (have && un < nunits) nxt = gather_unit(p, cs, un, unit, upt, lane);
         if (issued) {
-            if (!wait_mbar(&cs->gbar[lane], ph, w, SITE_GATHER_LOAD)) {
+            if (!wait_mbar(&cs->gbar[sl], ph, w, SITE_GATHER_LOAD)) {
                 ok = false;
                 // the load is in flight: give it a short, bounded chance to land
                 WaitCtx shortw{nullptr, 0u, 2000000LL};
-                wait_mbar(&cs->gbar[lane], ph, shortw, SITE_DRAIN);
+                wait_mbar(&cs->gbar[sl], ph, shortw, SITE_DRAIN);
             }
             ph ^= 1u;
             if (ok) bulk_store(p.xs + size_t(cur.row) * p.H, slot, row_bytes);

@@ -838,18 +838,11 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
     const int nunits = cs->tile_start[p.E] * upt;
     const int sl = min(warp * unit + lane, p.gather_slots - 1);  // this lane's slot (lanes >= unit never copy)
     uint8_t* slot = s + size_t(sl) * row_bytes;
-    // tiles [0, urgent] hold the rows of the first wave of work items
+    // tiles [0, urgent] hold the rows of the first wave of work items; worked
+    // out while the first unit's loads are in flight (it is first needed once
+    // they have landed)
     int urgent = -1;
-    {
-        const int nfirst = min(int(gridDim.x), cs->item_start[p.E]);
-        for (int i = lane; i < nfirst; i += 32) {
-            Info inf;
-            int gt;
-            decode_item(p, cs, i, inf, gt);
-            urgent = max(urgent, gt);
-        }
-        urgent = __reduce_max_sync(0xffffffffu, urgent);
-    }
+    bool urgent_known = false;
     uint32_t ph = 0;
     bool ok = true;
     int pend_tile = -1, pend_n = 0, pend_rows = 0;    // the unit whose stores may still be in flight
@@ -879,6 +872,17 @@ __device__ void gather_role(const Params& p, CtrlSmem* cs, const WaitCtx& w) {
         un = __shfl_sync(0xffffffffu, un, 0);
         GatherUnit nxt{-1, 0, 0, 0, -1};
         if (have && un < nunits) nxt = gather_unit(p, cs, un, unit, upt, lane);
+        if (!urgent_known) {
+            const int nfirst = min(int(gridDim.x), cs->item_start[p.E]);
+            for (int i = lane; i < nfirst; i += 32) {
+                Info inf;
+                int gt;
+                decode_item(p, cs, i, inf, gt);
+                urgent = max(urgent, gt);
+            }
+            urgent = __reduce_max_sync(0xffffffffu, urgent);
+            urgent_known = true;
+        }
         if (issued) {
             if (!wait_mbar(&cs->gbar[sl], ph, w, SITE_GATHER_LOAD)) {
                 ok = false;

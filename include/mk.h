@@ -249,10 +249,12 @@ size_t mk_ep_workspace_size(int T, int H, int F, int E, int k, int ranks);
  * weights are resident).  Copies the inputs in, runs the fused path, copies
  * the outputs back, and synchronises `stream` before returning, so the host
  * buffers are ready on return.  With the fused single-SM path, y_sorted goes
- * back in chunks of sorted rows (at most 64) while the kernel still runs: the
- * kernel raises a flag per finished chunk and a second, library-owned stream
- * waits on it and copies the chunk; other configurations copy after the
- * kernel.  Device staging comes from the library cache.  The library's
+ * back in chunks of sorted rows (whole 256-row tiles, at most 64 chunks)
+ * while the kernel still runs: the kernel raises a flag per finished chunk
+ * and a second, library-owned stream waits on the flags and copies the rows,
+ * in copies of 1, 1, 2, 4, ... chunks; other configurations copy after the
+ * kernel.  With cfg->n_group = 0 this call orders the work tile by tile
+ * (all N-blocks of a tile together), so rows complete in order.  Device staging comes from the library cache.  The library's
  * stream and chunk flags belong to (device, stream); calls on one stream run
  * one after another. */
 mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_host, int T, int H, int E,

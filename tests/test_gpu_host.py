@@ -61,9 +61,9 @@ def _device_call(x, l, Wd, k, cfg=None):
 
 
 @pytest.mark.parametrize("shape", [
-    (333, 128, 256, 8, 2),      # 666 rows: two chunks, the last ragged
+    (333, 128, 256, 8, 2),      # 666 rows: three chunks of 256, the last ragged; copies of 1, 1, 1
     (100, 128, 192, 4, 2),      # one chunk, partial N-block
-    (20000, 128, 128, 16, 2),   # 40000 rows: 64 chunks of 625
+    (20000, 128, 128, 16, 2),   # 40000 rows: 53 chunks of 768; copies of 1, 1, 2, 4, 8, 16, 21
     (5000, 256, 512, 64, 8),
 ], ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("out_dtype", [mk.MK_OUT_BF16, mk.MK_OUT_F32], ids=["bf16", "f32"])
@@ -123,3 +123,22 @@ def test_streamed_host_full_size_mixtral_like():
     d = _device_call(x, l, Wd, w.k)
     for key in d:
         np.testing.assert_array_equal(h[key], d[key])
+
+
+def test_host_entry_orders_work_tile_by_tile():
+    """With the work order left to the library, the host entry takes all
+    N-blocks of a tile together (groups as wide as the N-blocks), so its
+    streamed rows complete in order; a caller's group width is kept.  The
+    bytes equal the device path's, whose order groups N-blocks."""
+    T, H, F, E, k = 256, 4096, 8192, 2, 1  # 64 MiB of weights per expert: the device path groups 4 of 32 N-blocks
+    x, l, W = _inputs(T, H, F, E, k, seed=5)
+    Wd = gu.to_device(x, l, W)[2]
+    d = _device_call(x, l, Wd, k)
+    assert mk.mk_last_launch_info()["n_group"] == 4
+    st, h = _host_call(x, l, Wd, k)
+    assert st == mk.MK_OK and mk.mk_last_launch_info()["n_group"] == F // 256
+    for key in d:
+        np.testing.assert_array_equal(h[key], d[key])
+    st, h = _host_call(x, l, Wd, k, mk.make_config(n_group=8))
+    assert st == mk.MK_OK and mk.mk_last_launch_info()["n_group"] == 8
+    np.testing.assert_array_equal(h["y"], d["y"])

@@ -843,12 +843,11 @@ mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_ho
                 return MK_ERR_CUDA;
             if (ncopies > 0) g *= 2;
         }
-        if (cudaEventRecord(hs->copied, hs->copy) != cudaSuccess || cudaStreamWaitEvent(st, hs->copied, 0) != cudaSuccess)
-            return MK_ERR_CUDA;
         if (getenv("MK_LOG"))
             fprintf(stderr, "[mk] host entry: %d result chunks of %d rows streamed in %d copies, stream waits %s (%d)\n",
                     nchunks, srows, ncopies, waits ? "used" : "refused, copies follow the kernel", wait_err);
     }
+    // the small outputs follow the kernel on `stream`, beside the streamed rows
     if (cudaMemcpyAsync(expert_offsets_host, base + o_o, size_t(E + 1) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MK_ERR_CUDA;
     if (T > 0) {
@@ -857,15 +856,19 @@ mk_status_t mk_moe_dispatch_gemm_host(const void* x_host, const float* logits_ho
             cudaMemcpyAsync(gate_w_host, base + o_g, rows * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
             return MK_ERR_CUDA;
     }
+    if (streamed &&
+        (cudaEventRecord(hs->copied, hs->copy) != cudaSuccess || cudaStreamWaitEvent(st, hs->copied, 0) != cudaSuccess))
+        return MK_ERR_CUDA;
     return mk_get_status(stream);
 }
 
 mk_status_t mk_get_status(void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
-    if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
+    // the read of the error word is ordered after all of the stream's work,
+    // and synchronises with it
     uint32_t e[4] = {0, 0, 0, 0};
     if (read_and_clear_error(e, st) != cudaSuccess) return MK_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
     if (e[0] == ERR_NONE) return MK_OK;
     {
         std::lock_guard<std::mutex> lock(g_mu);
